@@ -1,0 +1,96 @@
+"""Seeded synthetic inputs for the W4A8 MoE layer and the block-FP8 projection.
+
+This module draws random numbers only; it holds none of the method's
+arithmetic (no quantization, routing or GEMM). The tests, the oracle and the
+benchmark all take their inputs from here, so both sides of every comparison
+see identical tensors.
+
+Workload shapes follow the layers the pages describe: Grok-1 (hidden 6144,
+intermediate 32768, 8 experts, 2 per token, bf16; "ROCm: enable
+trillion-parameter MoE models with INT4-FP8 single node", config.json),
+Mixtral-8x7B ("[AMD][Quantization] Add int4fp8_moe online quantization on
+ROCm", run command), and the block-FP8 dense projections [16384,2560],
+[13312,2560] ("qwen4_exp: serve the block-FP8 dense projections natively",
+description) plus an o_proj-shaped [2560,6144].
+
+Distributions: weights N(0, 0.02) rounded to bf16; activations N(0, 1) in bf16;
+router logits N(0, 1) in fp32, plus an optional per-expert logit bias that
+skews the expert load. One generator per call, drawn in a fixed order
+(logits, bias, x, gate_up, down).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+
+@dataclass(frozen=True)
+class MoEShape:
+    name: str
+    T: int
+    H: int
+    I: int
+    E: int
+    k: int
+    act: int            # 0 = SiLU-gated, 1 = GELU(tanh)-gated
+    bias_std: float     # std of the per-expert logit bias (0 = none)
+
+
+MOE_SHAPES = {
+    "tiny": MoEShape("tiny T16 H256 I512 E8 k2 SiLU", 16, 256, 512, 8, 2, 0, 0.0),
+    "mixtral_decode": MoEShape("Mixtral-8x7B MoE layer decode T32 H4096 I14336 E8 k2 SiLU", 32,
+                               4096, 14336, 8, 2, 0, 0.5),
+    "grok_decode": MoEShape("Grok-1 MoE layer decode T32 H6144 I32768 E8 k2 GELU-tanh", 32, 6144,
+                            32768, 8, 2, 1, 0.0),
+    "grok_decode_t8": MoEShape("Grok-1 MoE layer decode T8 H6144 I32768 E8 k2 GELU-tanh", 8, 6144,
+                               32768, 8, 2, 1, 0.0),
+    "grok_decode_t1": MoEShape("Grok-1 MoE layer decode T1 H6144 I32768 E8 k2 GELU-tanh", 1, 6144,
+                               32768, 8, 2, 1, 0.0),
+    "grok_prefill": MoEShape("Grok-1 MoE layer prefill T32768 H6144 I32768 E8 k2 GELU-tanh skewed",
+                             32768, 6144, 32768, 8, 2, 1, 1.0),
+}
+
+BLOCK_FP8_SHAPES = [(16384, 2560), (13312, 2560), (2560, 6144)]
+BLOCK_FP8_M = [1, 8, 64, 4096]
+
+
+def _gen(seed: int, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def moe_inputs(T: int, H: int, I: int, E: int, bias_std: float = 0.0, seed: int = 0,
+               device="cpu", weights: bool = True, weight_std: float = 0.02):
+    """Router logits fp32 [T,E] (bias added), x bf16 [T,H], W_gu bf16 [E,2I,H], W_d bf16 [E,H,I]."""
+    g = _gen(seed, device)
+    logits = torch.randn(T, E, generator=g, device=device, dtype=torch.float32)
+    bias = torch.randn(E, generator=g, device=device, dtype=torch.float32) * bias_std
+    if bias_std:
+        logits = logits + bias
+    x = torch.randn(T, H, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+    out = {"logits": logits.contiguous(), "x": x.contiguous()}
+    if weights:
+        w_gu = torch.empty(E, 2 * I, H, device=device, dtype=torch.bfloat16)
+        w_d = torch.empty(E, H, I, device=device, dtype=torch.bfloat16)
+        for e in range(E):  # per expert keeps the fp32 temporary small
+            w_gu[e] = (torch.randn(2 * I, H, generator=g, device=device) * weight_std).to(torch.bfloat16)
+        for e in range(E):
+            w_d[e] = (torch.randn(H, I, generator=g, device=device) * weight_std).to(torch.bfloat16)
+        out["w_gu"] = w_gu
+        out["w_d"] = w_d
+    return out
+
+
+def block_fp8_inputs(M: int, N: int, K: int, seed: int = 0, device="cpu", weight_std: float = 0.02):
+    """Activations x bf16 [M,K] and a dense weight bf16 [N,K] to be block-quantized."""
+    g = _gen(seed, device)
+    x = torch.randn(M, K, generator=g, device=device).to(torch.bfloat16)
+    w = (torch.randn(N, K, generator=g, device=device) * weight_std).to(torch.bfloat16)
+    return {"x": x.contiguous(), "w": w.contiguous()}
+
+
+def calibration_tokens(T: int, n: int = 8):
+    """Tokens the static intermediate scale is calibrated on: the first min(T, n)."""
+    return list(range(min(T, n)))
