@@ -1,0 +1,377 @@
+"""Benchmark of the W4A8 MoE layer on GB300.
+
+One step = one pass of the whole hot path over one batch of tokens: moe_route
+(softmax top-k, histogram, permutation) + moe_w4a8_forward (gather, grouped
+gate_up GEMM with gating and E4M3 requantization, grouped down GEMM, weighted
+combine), with the E4M3 activations and router logits resident in HBM. The
+default workload is the Mixtral-8x7B-shaped decode layer (32 tokens, hidden
+4096, intermediate 14336, 8 experts, top-2, SiLU-gated, per-expert logit bias
+N(0, 0.5)); --config selects another layer shape. Weights (705.7 MB packed for
+8 active experts) are far larger than L2, so every step streams them from HBM.
+
+Prints one JSON line (rank 0). `python bench.py --impl reference` times the CPU
+oracle on a bounded sample of the same workload instead.
+
+Multi-GPU (torchrun): every rank runs its own replica of the layer on its own
+tokens (the path has no exchange step), timed between barriers; value is the
+total tokens of all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "W4A8 MoE layer tokens/s"
+UNIT = "tokens/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="mixtral_decode")
+    ap.add_argument("--cpu-sample-tokens", type=int, default=0,
+                    help="tokens in the oracle sample (0: sized for ~15 s of CPU work)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- dist
+def dist_setup(n):
+    import torch
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi SM clock and throttle reasons sampled during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self._stop = threading.Event()
+        self._th = None
+
+    def _poll(self):
+        cmd = ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits"]
+        while not self._stop.is_set():
+            try:
+                out = subprocess.run(cmd, capture_output=True, text=True, timeout=5).stdout.strip()
+                if out:
+                    self.rows.append([c.strip() for c in out.split(",")])
+            except Exception:
+                pass
+            self._stop.wait(0.1)
+
+    def __enter__(self):
+        self._th = threading.Thread(target=self._poll, daemon=True)
+        self._th.start()
+        return self
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        self._th.join(timeout=10)
+        if not self.rows:  # region shorter than one poll: take one sample now
+            self._stop.clear()
+            self._stop.set()
+            cmd = ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                   "--format=csv,noheader,nounits"]
+            try:
+                out = subprocess.run(cmd, capture_output=True, text=True, timeout=5).stdout.strip()
+                if out:
+                    self.rows.append([c.strip() for c in out.split(",")])
+            except Exception:
+                pass
+
+    def summary(self):
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in self.rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in self.rows if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4)
+                          if len(r) > 3 + i and r[3 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(self.rows)}
+
+
+# ----------------------------------------------------------------------------- workload
+def algorithmic_bytes(shape, counts):
+    """Weight bytes the layer must read (experts with tokens only) plus activation I/O."""
+    H, I = shape.H, shape.I
+    active = sum(1 for c in counts if c > 0)
+    gate_up = active * (2 * I * H // 2 + 2 * I * 4)
+    down = active * (H * I // 2 + H * 4)
+    act_io = shape.T * H * (1 + 2)
+    return gate_up, down, act_io
+
+
+def static_hidden_scale(inp, shape, tokens=8):
+    """Static scale of the intermediate activation for the synthetic layer,
+    calibrated in float32 on the unquantized bf16 weights over the first tokens
+    (the offline calibration a static scheme implies)."""
+    import torch
+    x = inp["x"][:tokens].float()
+    top = torch.topk(inp["logits"][:tokens], shape.k, dim=1).indices
+    hmax = 0.0
+    for t in range(x.shape[0]):
+        for e in top[t].tolist():
+            gu = inp["w_gu"][e].float() @ x[t]
+            g, u = gu[:shape.I], gu[shape.I:]
+            a = torch.nn.functional.silu(g) if shape.act == 0 else \
+                torch.nn.functional.gelu(g, approximate="tanh")
+            hmax = max(hmax, float((a * u).abs().max()))
+    return hmax / 448.0 if hmax > 0 else 1.0
+
+
+def run_ours(args, rank, world):
+    import torch
+
+    import w4a8_moe_gb300 as lib
+    from w4a8_moe_gb300 import synth
+
+    shape = synth.MOE_SHAPES[args.config]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    inp = synth.moe_inputs(shape.T, shape.H, shape.I, shape.E, bias_std=shape.bias_std,
+                           seed=rank, device=dev)
+    w_gu, s_gu = lib.w4a8_quantize_experts(inp["w_gu"])
+    w_d, s_d = lib.w4a8_quantize_experts(inp["w_d"])
+    xq, a1 = lib.w4a8_quantize_act(inp["x"], compute_scale=True)      # calibration of a1
+    s2 = static_hidden_scale(inp, shape)
+    a2 = torch.tensor([s2], dtype=torch.float32, device=dev)
+    logits = inp["logits"]
+    x_bf16 = inp["x"]
+    del inp["w_gu"], inp["w_d"]
+    torch.cuda.empty_cache()
+
+    T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
+    route_ws = torch.zeros(lib.moe_route_workspace_size(T, E, k), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(lib.moe_w4a8_workspace_size(T, H, I, E, k), dtype=torch.uint8, device=dev)
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    route = lib.moe_route(logits, k, ws=route_ws)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        lib.moe_route(logits, k, out=route, ws=route_ws)
+        lib.moe_w4a8_forward(xq, a1, w_gu, s_gu, w_d, s_d, a2, shape.act, route, out=out, ws=ws)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    counts = route.counts.cpu().tolist()
+    gu_bytes, d_bytes, act_bytes = algorithmic_bytes(shape, counts)
+
+    # timed region: K steps between barriers, events on the launching stream;
+    # per-kernel events recorded by the library around the two GEMMs
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        start.record(stream)
+        for i in range(args.steps):
+            lib.w4a8_set_profile_events(ev[i])
+            step()
+        stop.record(stream)
+        lib.w4a8_set_profile_events(None)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms_total = start.elapsed_time(stop)
+    ms_total = max_over_ranks(ms_total, world)
+    ms_gu = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    ms_dn = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    assert lib.w4a8_device_error(ws) == 0, "device error word set"
+
+    # end to end through the public API with host buffers: H2D of the step's
+    # inputs (bf16 x, fp32 logits) from pinned memory, static-scale quantization,
+    # route, forward, D2H of the bf16 output
+    hx = x_bf16.cpu().pin_memory()
+    hl = logits.cpu().pin_memory()
+    hout = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+    dx = torch.empty_like(x_bf16)
+    dl = torch.empty_like(logits)
+
+    def e2e_step():
+        dx.copy_(hx, non_blocking=True)
+        dl.copy_(hl, non_blocking=True)
+        lib.w4a8_quantize_act(dx, scale=a1, compute_scale=False, out=xq)
+        lib.moe_route(dl, k, out=route, ws=route_ws)
+        lib.moe_w4a8_forward(xq, a1, w_gu, s_gu, w_d, s_d, a2, shape.act, route, out=out, ws=ws)
+        hout.copy_(out, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_steps = max(10, min(args.steps, 500))
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e_steps):
+        e2e_step()
+        torch.cuda.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+
+    res = {
+        "ms_per_step": ms_total / args.steps,
+        "value": world * T * args.steps / (ms_total / 1e3),
+        "e2e": {"value": world * T * e_steps / e2e_s, "unit": UNIT,
+                "h2d_bytes_per_step": hx.numel() * 2 + hl.numel() * 4,
+                "d2h_bytes_per_step": hout.numel() * 2},
+        "clocks": clk.summary(),
+        "kernels": {"gate_up_ms": ms_gu, "down_ms": ms_dn, "gate_up_bytes": gu_bytes,
+                    "down_bytes": d_bytes, "act_bytes": act_bytes,
+                    "active_experts": sum(1 for c in counts if c > 0)},
+        "shape": shape,
+    }
+    return res
+
+
+def cpu_baseline(args, shape):
+    """The oracle, as it stands, on a bounded sample of the same layer."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from w4a8_moe_gb300 import synth
+
+    # same seeded layer as rank 0 of the GPU arm (drawn on the GPU when there is one)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = synth.moe_inputs(shape.T, shape.H, shape.I, shape.E, bias_std=shape.bias_std, seed=0,
+                           device=dev)
+    inp = {k_: v.cpu() for k_, v in inp.items()}
+    if dev == "cuda":
+        torch.cuda.empty_cache()
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    pgu, sgu = oracle.quantize_experts(bits(inp["w_gu"]))
+    pd, sd = oracle.quantize_experts(bits(inp["w_d"]))
+    s1 = oracle.act_scale(bits(inp["x"]))
+    xq = oracle.quantize_act(bits(inp["x"]), s1)
+    threads = oracle.cores()
+    ids, w = oracle.route(inp["logits"].numpy(), shape.k)
+    oracle.permute(ids, shape.E)
+    s2 = oracle.moe_hidden_scale(xq, s1, pgu, sgu, shape.act, ids, [0], nthreads=threads)
+    # size the sample for ~15 s of CPU work: time one token first
+    t0 = time.perf_counter()
+    oracle.moe_forward(xq, s1, pgu, sgu, pd, sd, s2, shape.act, ids, w, tokens=[0], nthreads=1)
+    one = time.perf_counter() - t0
+    n = args.cpu_sample_tokens or max(1, min(shape.T, int(15.0 * threads / max(one, 1e-6))))
+    toks = list(range(n))
+    t0 = time.perf_counter()
+    oracle.route(inp["logits"].numpy()[:n], shape.k)
+    oracle.moe_forward(xq, s1, pgu, sgu, pd, sd, s2, shape.act, ids, w, tokens=toks, nthreads=threads)
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{n} of {shape.T} tokens of the {shape.name} layer (route + exact-integer "
+                      f"MoE forward), {threads} threads"}
+
+
+def config_dict(shape, world):
+    return {"workload": shape.name, "tokens_per_step": shape.T, "hidden": shape.H,
+            "intermediate": shape.I, "experts": shape.E, "top_k": shape.k,
+            "activation": "SiLU-gated" if shape.act == 0 else "GELU-tanh-gated",
+            "global_batch": shape.T * world, "parallelism": f"replicas{world}",
+            "l2": "weights (packed) larger than L2; no flush needed"}
+
+
+def main():
+    args = parse()
+    rank, world = dist_setup(args.gpus)
+    from w4a8_moe_gb300 import synth
+    shape = synth.MOE_SHAPES[args.config]
+
+    if args.impl == "reference":
+        if rank == 0:
+            cb = cpu_baseline(args, shape)
+            line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT,
+                    "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                    "ms_per_step": shape.T / cb["value"] * 1e3, "higher_is_better": True,
+                    "scaling": "weak", "vs_baseline": None, "dtype": "int64+f64",
+                    "data": "synthetic", "config": config_dict(shape, 1),
+                    "cpu_baseline": cb,
+                    "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0,
+                            "d2h_bytes_per_step": 0}}
+            print(json.dumps(line), flush=True)
+        return
+
+    import json as _json  # noqa: F401
+    sys.path.insert(0, ROOT)
+    import __graft_entry__
+    __graft_entry__.build()
+    res = run_ours(args, rank, world)
+    if rank != 0:
+        return
+    peaks = {}
+    pp = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pp):
+        peaks = json.load(open(pp))
+    hbm_peak = peaks.get("hbm_gbs", 6800.0)
+    kk = res["kernels"]
+    gu_gbs = kk["gate_up_bytes"] / (kk["gate_up_ms"] * 1e-3) / 1e9
+    roof = {"bound": "hbm", "kernel": "moe_gemm_kernel<gate_up>", "achieved": gu_gbs,
+            "peak": hbm_peak, "unit": "GB/s", "frac": gu_gbs / hbm_peak,
+            "peak_source": "MEASURED_PEAKS.json hbm_gbs (burst copy)" if peaks else "fallback 6.8 TB/s",
+            "traffic": None,
+            "per_launch_ms": kk["gate_up_ms"], "algorithmic_bytes": kk["gate_up_bytes"],
+            "down": {"per_launch_ms": kk["down_ms"], "algorithmic_bytes": kk["down_bytes"],
+                     "achieved": kk["down_bytes"] / (kk["down_ms"] * 1e-3) / 1e9}}
+    layer_bytes = kk["gate_up_bytes"] + kk["down_bytes"] + kk["act_bytes"]
+    line = {"metric": METRIC, "value": res["value"], "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3xint4->f32",
+            "data": "synthetic", "config": config_dict(shape, world),
+            "layer_weight_gbs": layer_bytes / (res["ms_per_step"] * 1e-3) / 1e9,
+            "layer_hbm_frac": layer_bytes / (res["ms_per_step"] * 1e-3) / 1e9 / hbm_peak,
+            "roofline": roof, "e2e": res["e2e"], "clocks": res["clocks"],
+            "gpu_launches": 5 * args.steps}
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args, shape)
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

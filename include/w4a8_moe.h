@@ -1,0 +1,190 @@
+/*
+ * w4a8_moe.h -- C ABI of the GB300 (sm_103a) W4A8 mixture-of-experts library.
+ *
+ * The library computes the W4A8 MoE FFN of the pages
+ *   "ROCm: enable trillion-parameter MoE models with INT4-FP8 single node"
+ *       (sglang PR #4152; Motivation and config.json quantization_config), and
+ *   "[AMD][Quantization] Add int4fp8_moe online quantization on ROCm"
+ *       (sglang PR #7392; description and review summary),
+ * and the block-FP8 dense projection of
+ *   "qwen4_exp: serve the block-FP8 dense projections natively (+25% decode)"
+ *       (FreeToken PR #392; description and "What").
+ *
+ * Conventions shared by every call
+ *  - Pointers are DEVICE pointers to caller-owned memory unless stated. The
+ *    library never allocates, frees or synchronizes; every call only enqueues
+ *    kernels on `stream` (a cudaStream_t passed as void*, NULL = legacy
+ *    default stream) and returns.
+ *  - Arrays are row-major and contiguous; every pointer must be 16-byte
+ *    aligned (W4A8_ERR_ALIGN otherwise).
+ *  - bf16 is passed as uint16_t bit patterns; fp8 is OCP E4M3 ("fn": max 448,
+ *    no infinity) as uint8_t codes.
+ *  - Arguments are validated on the host before anything is enqueued; on an
+ *    error nothing is launched and the status says why. No C++ exception
+ *    crosses the ABI.
+ *  - The library needs a GB300-class GPU (compute capability 10.3); on any
+ *    other device, or without a device, calls return W4A8_ERR_DEVICE. There is
+ *    no CPU fallback.
+ *  - Workspace: calls that take `ws` need ws_bytes >= the matching
+ *    *_workspace_size(). The first 256 bytes of every workspace hold a device
+ *    error word; the caller zero-fills a workspace once when it allocates it.
+ *    Kernels only OR bits into that word (a bounded wait that ran out sets
+ *    bit 0); w4a8_device_error() reads and clears it.
+ *  - Stateless and thread-safe; concurrent calls must use distinct workspaces.
+ */
+#ifndef W4A8_MOE_H
+#define W4A8_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    W4A8_OK = 0,
+    W4A8_ERR_NULL = 1,      /* a required pointer is NULL                      */
+    W4A8_ERR_SHAPE = 2,     /* a size is out of the supported range            */
+    W4A8_ERR_ALIGN = 3,     /* a pointer is not 16-byte aligned                */
+    W4A8_ERR_WORKSPACE = 4, /* ws is NULL or ws_bytes is too small             */
+    W4A8_ERR_DEVICE = 5,    /* no sm_103 device, or the kernel image is absent */
+    W4A8_ERR_LAUNCH = 6,    /* a CUDA launch or driver call failed             */
+    W4A8_ERR_TIMEOUT = 7    /* reported by w4a8_device_error: a bounded wait ran out */
+} w4a8_status_t;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* w4a8_status_string(int status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int w4a8_version(void);
+
+/*
+ * w4a8_quantize_experts -- column-wise symmetric INT4 quantization of expert
+ * weights, 8 codes packed per int32 (PR #7392 review summary, "Core
+ * Quantization Utilities": column-wise INT4 quantization and INT4 -> INT32
+ * packing; PR #4152 config.json int4_experts {bits 4, sym true, group column}).
+ *
+ *   w_bf16 [E, N, K] bf16  : weights, output channel n, reduction index k.
+ *   packed [E, N, K/8] i32 : out. Code k = 8j+i sits in bits 4i..4i+3 of word j
+ *                            as a two's-complement nibble.
+ *   scale  [E, N] fp32     : out. s = max_k |w| / 7 (1 for an all-zero row).
+ *   Codes: q = clamp(rint(w / s), -8, 7), fp32 division, ties to even.
+ *   Requires E >= 1, N >= 1, K a positive multiple of 8. Offline step (no ws).
+ */
+int w4a8_quantize_experts(const uint16_t* w_bf16, int E, int N, int K, int32_t* packed,
+                          float* scale, void* stream);
+
+/*
+ * w4a8_quantize_act -- per-tensor ("tensor-wise", PR #7392 review summary)
+ * FP8 quantization of activations with a static scale (PR #4152
+ * quantization_config, activation_scheme "static").
+ *
+ *   x_bf16 [numel] bf16, numel a positive multiple of 16.
+ *   scale  [1] fp32 (device). compute_scale = 1: calibrate, writes
+ *          scale = max|x| / 448 (1 if x is all zero) and uses it;
+ *          compute_scale = 0: reads the static scale.
+ *   x_e4m3 [numel] u8: out, E4M3(x / scale) with fp32 division, RNE, +-448.
+ *   ws: w4a8_quantize_act_workspace_size(numel) bytes (needed when
+ *       compute_scale = 1; may be NULL with ws_bytes = 0 otherwise).
+ */
+int w4a8_quantize_act(const uint16_t* x_bf16, int64_t numel, float* scale, int compute_scale,
+                      uint8_t* x_e4m3, void* ws, size_t ws_bytes, void* stream);
+size_t w4a8_quantize_act_workspace_size(int64_t numel);
+
+/*
+ * moe_route -- softmax top-k routing with renormalized weights, expert
+ * histogram and stable token permutation (the MoE gate of PR #4152 stays
+ * unquantized: ignored_layers; num_experts_per_tok = k).
+ *
+ *   logits [T, E] fp32 : router logits (any bias already added).
+ *   topk_ids [T, k] i32 : out. The k largest logits, descending; equal logits
+ *                         are ranked by lower expert index.
+ *   topk_w [T, k] fp32  : out. softmax(logits)[ids]; with renormalize = 1
+ *                         divided by their sum (so each row sums to 1).
+ *   counts [E] i32      : out. Assignments per expert.
+ *   offsets [E+1] i32   : out. Exclusive prefix sum of counts; offsets[E] = T*k.
+ *   sorted_ids [T*k] i32: out. Assignment a = t*k + j placed at
+ *                         offsets[e] + (number of earlier assignments to e).
+ *   inv_perm [T*k] i32  : out. inv_perm[sorted_ids[p]] = p.
+ *   Requires T >= 1, 1 <= k <= E <= 256, T*k < 2^31.
+ *   ws: moe_route_workspace_size(T, E, k) bytes.
+ */
+int moe_route(const float* logits, int T, int E, int k, int renormalize, int32_t* topk_ids,
+              float* topk_w, int32_t* counts, int32_t* offsets, int32_t* sorted_ids,
+              int32_t* inv_perm, void* ws, size_t ws_bytes, void* stream);
+size_t moe_route_workspace_size(int T, int E, int k);
+
+/*
+ * moe_w4a8_forward -- the W4A8 MoE FFN (PR #7392 description: INT4 expert
+ * weights upcast to FP8 so that FP8 math is used; PR #4152 Motivation: FP8
+ * tensor cores, INT4 weights for lower memory bandwidth).
+ *
+ * For every assignment a = (t, j) with expert e = topk_ids[t, j]:
+ *   gate_i = a1 * S_gu[e, i]     * sum_h x[t,h] q_gu[e, i, h]         (i < I)
+ *   up_i   = a1 * S_gu[e, I + i] * sum_h x[t,h] q_gu[e, I + i, h]
+ *   h_i    = act(gate_i) * up_i,  act = SiLU (act = 0) or GELU-tanh (act = 1)
+ *   hq_i   = E4M3(h_i / a2)                                    (static scale a2)
+ *   y_n    = a2 * S_d[e, n] * sum_i hq_i q_d[e, n, i]
+ *   out[t, n] = bf16( sum_j topk_w[t, j] * y_n(t, j) )
+ * with x = dec(x_e4m3) and fp32 tensor-core accumulation.
+ *
+ *   x_e4m3 [T, H] u8; a1_scale [1] fp32; a2_scale [1] fp32 (device pointers).
+ *   w_gu [E, 2I, H/8] i32 and s_gu [E, 2I] fp32 from w4a8_quantize_experts of
+ *        a [E, 2I, H] weight whose rows [0, I) are the gate, [I, 2I) the up.
+ *   w_d  [E, H, I/8] i32 and s_d [E, H] fp32.
+ *   topk_ids, topk_w, counts, offsets, sorted_ids, inv_perm: from moe_route.
+ *   out_bf16 [T, H] bf16: out.
+ *   Requires H and I positive multiples of 256, 1 <= k <= E <= 256, T >= 1.
+ *   ws: moe_w4a8_workspace_size(T, H, I, E, k) bytes.
+ */
+int moe_w4a8_forward(const uint8_t* x_e4m3, const float* a1_scale, int T, int H, int I, int E,
+                     int k, const int32_t* w_gu, const float* s_gu, const int32_t* w_d,
+                     const float* s_d, const float* a2_scale, int act, const int32_t* topk_ids,
+                     const float* topk_w, const int32_t* counts, const int32_t* offsets,
+                     const int32_t* sorted_ids, const int32_t* inv_perm, uint16_t* out_bf16,
+                     void* ws, size_t ws_bytes, void* stream);
+size_t moe_w4a8_workspace_size(int T, int H, int I, int E, int k);
+
+/*
+ * fp8_block_linear -- block-FP8 dense projection y = x W^T (PR #392
+ * description: FP8_PB_WO weights consumed with their weight_scale_inv, one
+ * fp32 scale per 128-row x 128-col block).
+ *
+ *   x_bf16 [M, K] bf16: activations, quantized inside the call per token and
+ *          128-column group g: xs[m, g] = max|x| / 448 (1 if zero),
+ *          xq = E4M3(x / xs).
+ *   w_e4m3 [N, K] u8; w_scale_inv [N/128, K/128] fp32: w ~ dec(w_e4m3) * Wsi.
+ *   y_bf16 [M, N] bf16: out, y[m, n] = sum_g xs[m,g] Wsi[n/128,g]
+ *          sum_{k in g} dec(xq[m,k]) dec(w[n,k]), fp32 accumulation.
+ *   xq_out [M, K] u8 and xs_out [M, K/128] fp32: optional outputs (may be NULL).
+ *   Requires M >= 1, N and K positive multiples of 128.
+ *   ws: fp8_block_linear_workspace_size(M, N, K) bytes.
+ */
+int fp8_block_linear(const uint16_t* x_bf16, int M, int N, int K, const uint8_t* w_e4m3,
+                     const float* w_scale_inv, uint16_t* y_bf16, uint8_t* xq_out, float* xs_out,
+                     void* ws, size_t ws_bytes, void* stream);
+size_t fp8_block_linear_workspace_size(int M, int N, int K);
+
+/*
+ * w4a8_set_profile_events -- measurement hook (not part of the method). Sets,
+ * for the calling host thread, up to four cudaEvent_t handles that
+ * moe_w4a8_forward records on its stream: [0] before the gate_up GEMM,
+ * [1] after it, [2] after the down GEMM, [3] after the final combine.
+ * count = 0 (or events = NULL) switches recording off. Returns W4A8_OK, or
+ * W4A8_ERR_SHAPE for count outside 0..4.
+ */
+int w4a8_set_profile_events(void* const* events, int count);
+
+/*
+ * w4a8_device_error -- read and clear the device error word of a workspace.
+ * Synchronizes `stream` (the only call that does). *code_out receives
+ * W4A8_OK, or W4A8_ERR_TIMEOUT when a kernel gave up on a bounded wait since
+ * the last read. Returns W4A8_OK or W4A8_ERR_NULL / W4A8_ERR_LAUNCH.
+ */
+int w4a8_device_error(void* ws, int* code_out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* W4A8_MOE_H */

@@ -1,0 +1,117 @@
+"""CPU-only checks of the C ABI: the library builds for sm_103a, loads, exports
+every symbol include/w4a8_moe.h declares, validates arguments on the host
+before touching a device, and refuses to run without an sm_103 GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from helpers import ROOT, ensure_built
+
+HEADER = os.path.join(ROOT, "include", "w4a8_moe.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z][a-z0-9_]+)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in {"if", "while", "sizeof"}))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = ensure_built()
+    return ctypes.CDLL(path)
+
+
+def test_header_lists_the_entry_points():
+    names = declared_functions()
+    for required in ["w4a8_quantize_experts", "w4a8_quantize_act", "moe_route", "moe_w4a8_forward",
+                     "fp8_block_linear", "moe_w4a8_workspace_size", "w4a8_status_string",
+                     "w4a8_device_error"]:
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_library_targets_sm103a_only():
+    from w4a8_moe_gb300 import build as b
+    assert b.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_status_strings(lib):
+    lib.w4a8_status_string.restype = ctypes.c_char_p
+    for code in range(8):
+        assert lib.w4a8_status_string(code).startswith(b"W4A8")
+    assert lib.w4a8_version() >= 100
+
+
+def _vp(v):
+    return ctypes.c_void_p(v)
+
+
+def test_validation_happens_before_the_device(lib):
+    """Null, shape, alignment and workspace errors come back without a GPU;
+    a valid call without a GPU is W4A8_ERR_DEVICE (no CPU fallback)."""
+    P, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    f = lib.moe_route
+    f.argtypes = [P, i32, i32, i32, i32, P, P, P, P, P, P, P, sz, P]
+    f.restype = i32
+    good = _vp(0x10000)
+    ws_need = lib.moe_route_workspace_size(32, 8, 2)
+    # NULL
+    assert f(None, 32, 8, 2, 1, good, good, good, good, good, good, good, ws_need, None) == 1
+    # shape: k > E, E > 256, T < 1
+    assert f(good, 32, 8, 9, 1, good, good, good, good, good, good, good, ws_need, None) == 2
+    assert f(good, 32, 300, 2, 1, good, good, good, good, good, good, good, 10**9, None) == 2
+    assert f(good, 0, 8, 2, 1, good, good, good, good, good, good, good, ws_need, None) == 2
+    # alignment
+    assert f(_vp(0x10004), 32, 8, 2, 1, good, good, good, good, good, good, good, ws_need, None) == 3
+    # workspace too small
+    assert f(good, 32, 8, 2, 1, good, good, good, good, good, good, good, 16, None) == 4
+    # everything valid, no GPU here (or a GPU that is not sm_103): device error
+    if not torch.cuda.is_available():
+        assert f(good, 32, 8, 2, 1, good, good, good, good, good, good, good, ws_need, None) == 5
+
+
+def test_forward_shape_rules(lib):
+    P, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    f = lib.moe_w4a8_forward
+    f.argtypes = [P, P, i32, i32, i32, i32, i32, P, P, P, P, P, i32, P, P, P, P, P, P, P, P, sz, P]
+    f.restype = i32
+    lib.moe_w4a8_workspace_size.restype = sz
+    g = _vp(0x10000)
+    ws = lib.moe_w4a8_workspace_size(32, 4096, 14336, 8, 2)
+    args = lambda T, H, I, E, k, act=0: [g, g, T, H, I, E, k, g, g, g, g, g, act, g, g, g, g, g, g, g,
+                                         g, ws, None]
+    assert f(*args(32, 4096 + 128, 14336, 8, 2)) == 2      # H not a multiple of 256
+    assert f(*args(32, 4096, 14336 + 128, 8, 2)) == 2      # I not a multiple of 256
+    assert f(*args(32, 4096, 14336, 8, 3, act=2)) == 2     # unknown activation
+    assert f(*args(32, 4096, 14336, 2, 3)) == 2            # k > E
+    bad = args(32, 4096, 14336, 8, 2)
+    bad[7] = _vp(0x10008)
+    assert f(*bad) == 3
+
+
+def test_workspace_sizes_are_monotone(lib):
+    lib.moe_w4a8_workspace_size.restype = ctypes.c_size_t
+    lib.fp8_block_linear_workspace_size.restype = ctypes.c_size_t
+    a = lib.moe_w4a8_workspace_size(32, 4096, 14336, 8, 2)
+    b = lib.moe_w4a8_workspace_size(64, 4096, 14336, 8, 2)
+    assert 256 < a < b
+    # decode: hq + gathered x + split-K partials; prefill-sized grows with T
+    assert lib.moe_w4a8_workspace_size(32768, 6144, 32768, 8, 2) > 4 * 10**9
+    assert lib.fp8_block_linear_workspace_size(1, 16384, 2560) > 2560
+
+
+def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    import w4a8_moe_gb300 as pkg
+    monkeypatch.setattr(pkg, "_lib", None)
+    monkeypatch.setattr(pkg, "_LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(pkg.W4A8Error):
+        pkg.moe_route_workspace_size(4, 8, 2)

@@ -1,0 +1,129 @@
+"""GPU parity of the W4A8 MoE forward against the oracle on the same seeded
+inputs: integer stages bit-exact, the bf16 output within rel-L2 <= 2e-3 and
+max-abs <= 1e-2 * max|ref| of the oracle's float64 result."""
+import numpy as np
+import pytest
+import torch
+
+from helpers import MoECase, QuantizedWeights, assert_close, bf16_to_f64, ensure_built
+from w4a8_moe_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+
+
+def run_case(case: MoECase, tokens=None, what=""):
+    case.check_integer_parts()
+    out = case.run_gpu()
+    ref = case.oracle_out(tokens)
+    got = bf16_to_f64(out if tokens is None else out[list(tokens)])
+    return assert_close(got, ref, what)
+
+
+def test_tiny_layer_all_tokens():
+    s = synth.MOE_SHAPES["tiny"]
+    case = MoECase(s.T, s.H, s.I, s.E, s.k, s.act)
+    run_case(case, what="tiny")
+
+
+@pytest.mark.parametrize("T,H,I,E,k,act", [
+    (1, 256, 256, 8, 2, 0),       # single token
+    (3, 256, 512, 2, 1, 1),       # k = 1, two experts, GELU
+    (33, 256, 256, 8, 2, 0),      # ragged: 64-token tile
+    (100, 512, 256, 4, 2, 1),     # 128-token tile
+    (300, 256, 256, 8, 2, 0),     # 256-token tiles, several per expert
+    (7, 256, 256, 1, 1, 0),       # E = 1, k = 1: dense W4A8 MLP
+    (64, 768, 512, 16, 4, 1),     # k = 4, 16 experts, H not a power of two
+])
+def test_shapes_and_tails(T, H, I, E, k, act):
+    case = MoECase(T, H, I, E, k, act, seed=T + E)
+    run_case(case, what=f"T{T} H{H} I{I} E{E} k{k}")
+
+
+def test_empty_experts_and_one_hot_expert():
+    T, E = 50, 8
+    logits = torch.randn(T, E, generator=torch.Generator().manual_seed(3))
+    logits[:, 2] = -50.0           # never routed
+    logits[:, 6] = -50.0
+    case = MoECase(T, 256, 256, E, 2, 0, logits_override=logits)
+    assert case.o_counts[2] == 0 and case.o_counts[6] == 0
+    run_case(case, what="empty experts")
+    logits1 = torch.zeros(40, E)
+    logits1[:, 4] = 20.0           # every token on expert 4 (k = 1)
+    case1 = MoECase(40, 256, 256, E, 1, 1, logits_override=logits1)
+    assert case1.o_counts[4] == 40
+    run_case(case1, what="one expert")
+
+
+def test_deterministic_and_error_word_clean():
+    import w4a8_moe_gb300 as lib
+    case = MoECase(37, 512, 512, 8, 2, 1, seed=9)
+    ws = torch.zeros(lib.moe_w4a8_workspace_size(37, 512, 512, 8, 2), dtype=torch.uint8,
+                     device="cuda")
+    a = case.run_gpu(ws=ws).clone()
+    b = case.run_gpu(ws=ws).clone()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert lib.w4a8_device_error(ws) == 0
+
+
+def _sample_tokens(case: MoECase, n: int):
+    """A few tokens that between them touch the most and the least loaded expert."""
+    ids = case.o_ids
+    counts = case.o_counts
+    live = [e for e in range(case.E) if counts[e] > 0]
+    pick = []
+    for e in (min(live, key=lambda e: counts[e]), max(live, key=lambda e: counts[e])):
+        t = int(np.nonzero((ids == e).any(1))[0][-1])
+        if t not in pick:
+            pick.append(t)
+    rng = np.random.default_rng(0)
+    for t in rng.permutation(case.T):
+        if len(pick) >= n:
+            break
+        if int(t) not in pick:
+            pick.append(int(t))
+    return sorted(pick)
+
+
+def test_mixtral_decode_full_size():
+    s = synth.MOE_SHAPES["mixtral_decode"]
+    case = MoECase(s.T, s.H, s.I, s.E, s.k, s.act, bias_std=s.bias_std)
+    case.check_integer_parts()
+    toks = _sample_tokens(case, 6)
+    out = case.run_gpu()
+    assert_close(bf16_to_f64(out[toks]), case.oracle_out(toks), "mixtral decode")
+
+
+@pytest.fixture(scope="module")
+def grok_weights():
+    s = synth.MOE_SHAPES["grok_decode"]
+    w = synth.moe_weights(s.H, s.I, s.E, device="cuda")
+    q = QuantizedWeights(w["w_gu"], w["w_d"])
+    del w
+    torch.cuda.empty_cache()
+    return q
+
+
+@pytest.mark.parametrize("name", ["grok_decode", "grok_decode_t8", "grok_decode_t1"])
+def test_grok_decode_full_size(name, grok_weights):
+    s = synth.MOE_SHAPES[name]
+    case = MoECase(s.T, s.H, s.I, s.E, s.k, s.act, bias_std=s.bias_std, weights=grok_weights)
+    case.check_integer_parts(sample_rows=[(0, 0), (3, 40000), (7, 65535)])
+    toks = _sample_tokens(case, 3)
+    out = case.run_gpu()
+    assert_close(bf16_to_f64(out[toks]), case.oracle_out(toks), name)
+
+
+def test_grok_prefill_full_size_sampled(grok_weights):
+    s = synth.MOE_SHAPES["grok_prefill"]
+    case = MoECase(s.T, s.H, s.I, s.E, s.k, s.act, bias_std=s.bias_std, weights=grok_weights)
+    case.check_integer_parts(sample_rows=[(1, 5)])
+    assert case.o_counts.max() > 2 * case.o_counts.min()       # skewed load
+    toks = _sample_tokens(case, 4) + [s.T - 1]
+    out = case.run_gpu()
+    assert torch.isfinite(out.float()).all()
+    assert_close(bf16_to_f64(out[toks]), case.oracle_out(toks), "grok prefill")

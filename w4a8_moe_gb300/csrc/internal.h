@@ -1,0 +1,78 @@
+// Host-side launchers shared between the C-ABI layer (api.cu) and the kernel
+// translation units. Every launcher only enqueues work on `s` and returns the
+// launch status.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace w4a8 {
+
+// ---- quant.cu
+cudaError_t launch_quantize_experts(const uint16_t* w, int E, int N, int K, int32_t* packed,
+                                    float* scale, cudaStream_t s);
+int act_amax_blocks(int64_t numel);
+cudaError_t launch_act_amax(const uint16_t* x, int64_t numel, float* partial, int nblocks,
+                            cudaStream_t s);
+cudaError_t launch_act_encode(const uint16_t* x, int64_t numel, float* scale, int compute_scale,
+                              const float* partial, int nblocks, uint8_t* out, cudaStream_t s);
+cudaError_t launch_block_act_quant(const uint16_t* x, int M, int K, uint8_t* xq, float* xs_rowmajor,
+                                   float* xs_t, int ld_t, cudaStream_t s);
+
+// ---- route.cu
+constexpr int kRouteChunk = 2048;         // assignments per histogram/scatter block
+constexpr int kRouteFusedMax = 4096;      // T*k up to which one block does everything
+cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, int32_t* ids,
+                         float* w, int32_t* counts, int32_t* offsets, int32_t* sorted_ids,
+                         int32_t* inv, int32_t* block_hist, int32_t* block_base, cudaStream_t s);
+
+// ---- moe.cu
+struct MoeConfig {
+    int bn;        // token tile (MMA N upper bound)
+    int kc;        // K elements per pipeline stage
+    int ksplit;    // split of the down projection's K
+};
+MoeConfig moe_pick_config(int T, int H, int I, int E, int k, int num_sms);
+int moe_ksplit_max(int T, int k);
+struct MoeLaunch {
+    const uint8_t* xq; const float* a1; int T, H, I, E, k;
+    const int32_t* w_gu; const float* s_gu; const int32_t* w_d; const float* s_d;
+    const float* a2; int act;
+    const int32_t* ids; const float* topk_w; const int32_t* counts; const int32_t* offsets;
+    const int32_t* sorted_ids; const int32_t* inv;
+    uint16_t* out;
+    // workspace pieces
+    uint8_t* xp; long long* s0x; uint8_t* hq; unsigned long long* s0h; float* ypart;
+    uint32_t* err;
+    void* events[4];  // optional cudaEvent_t recorded around the GEMMs
+};
+int launch_moe_forward(const MoeLaunch& L, const MoeConfig& cfg, int num_sms, cudaStream_t s);
+
+// ---- block_fp8.cu
+struct BlkConfig {
+    int bn;
+    int ksplit;
+};
+BlkConfig blk_pick_config(int M, int N, int K, int num_sms);
+int blk_ksplit_max(int M, int K);
+struct BlkLaunch {
+    int M, N, K;
+    const uint8_t* w; const float* wsi; uint16_t* y;
+    const uint8_t* xq; const float* xs_t; int ld_t;
+    float* ypart; uint32_t* err;
+};
+int launch_block_gemm(const BlkLaunch& L, const BlkConfig& cfg, int num_sms, cudaStream_t s);
+
+// ---- api.cu (tensor-map encoding through the driver entry point)
+bool encode_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
+                   uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows,
+                   CUtensorMapSwizzle swz);
+
+// Status codes mirrored from the public header for use inside the library.
+enum {
+    kOK = 0, kErrNull = 1, kErrShape = 2, kErrAlign = 3, kErrWorkspace = 4, kErrDevice = 5,
+    kErrLaunch = 6, kErrTimeout = 7
+};
+
+}  // namespace w4a8

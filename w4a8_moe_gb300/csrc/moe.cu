@@ -1,0 +1,696 @@
+// W4A8 MoE forward on sm_103a: gather -> grouped gate_up GEMM (+SiLU/GELU
+// gating, E4M3 requantization) -> grouped down GEMM -> weighted combine.
+//
+// "[AMD][Quantization] Add int4fp8_moe online quantization on ROCm",
+// description: the int4 MoE weights are upcast to float8 so that fp8 math is
+// used; "ROCm: enable trillion-parameter MoE models with INT4-FP8 single
+// node", Motivation: INT4 weights lower the memory bandwidth of decoding, the
+// FP8 tensor cores do the math.
+//
+// Grouped GEMM design (one persistent CTA per SM, 12 warps):
+//   warp 0      TMA producer: packed INT4 weight tile [128 rows x KC/2 bytes]
+//               and the expert's activation tile [BN tokens x KC] per stage.
+//   warp 1      TMEM owner + single-thread tcgen05.mma issuer.
+//   warps 4-7   converters: thread r owns A row r; it turns its packed
+//               nibbles into E4M3 bytes in the 128-byte-swizzled K-major layout
+//               the MMA reads.
+//   warps 8-11  epilogue: tcgen05.ld of the fp32 accumulator (lane = weight
+//               row, column = token), scales, activation, stores.
+// The MMA runs "swapped": M = 128 weight rows, N = the expert's tokens, so a
+// decode step with a handful of tokens per expert still uses M = 128 and the
+// weights stream through the SMs once.
+//
+// INT4 -> E4M3 upcast. A nibble n holds q = n - 16*(n >= 8). The byte
+// o = n ^ 8 = q + 8 lies in 0..15, and the E4M3 codes 0x00..0x0F encode
+// exactly o * 2^-9 (subnormals plus the first normal binade share the spacing
+// 2^-9). So one AND+XOR per 4 weights yields operands worth (q + 8) * 2^-9 and
+//   sum_h x_h q_h = 512 * sum_h x_h dec(o_h) - 8 * sum_h x_h,
+// where the per-token sum_h x_h is exact integer bookkeeping (S0 below). The
+// tensor-core product is the exact upcast the pages describe, shifted by a
+// constant that the epilogue removes.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace w4a8 {
+
+struct MoeGemmParams {
+    const int32_t* counts;   // [E]
+    const int32_t* offsets;  // [E+1]
+    int E;
+    int rows_per_expert;     // 2I (gate_up) or H (down)
+    int rt_count;            // 128-row weight tiles per expert
+    int kblocks;             // pipeline stages per tile (KC elements each)
+    int ksplit;              // splits of K (down only)
+    int I, H, A;
+    // gate_up epilogue
+    const float* s_gu;       // [E, 2I]
+    const float* a1;         // [1]
+    const float* a2;         // [1]
+    int act;
+    const long long* s0x;    // [A] sum_h 512*dec(x) of the assignment's token
+    uint8_t* hq;             // [A, I]
+    unsigned long long* s0h; // [A] sum_i 512*dec(hq), accumulated by atomics
+    // down epilogue
+    float* ypart;            // [ksplit, A, H] raw accumulator (before shift removal)
+    uint32_t* err;
+};
+
+template <int MODE, int BN, int KC, int PST, int AST>
+struct MoeTraits {
+    static constexpr int kAtoms = KC / 128;
+    static constexpr int kWBytes = 128 * KC / 2;
+    static constexpr int kBBytes = kAtoms * BN * 128;
+    static constexpr int kPBytes = kWBytes + kBBytes;
+    static constexpr int kABytes = kAtoms * 128 * 128;
+    static constexpr int kData = PST * kPBytes + AST * kABytes;
+    static constexpr int kBars = 2 * PST + 2 * AST + 4 + 1;  // + drain barrier
+    static constexpr int kCtrl = kBars * 8 + 16 + 4 * (256 + 260 + 260);
+    static constexpr int kSmem = 1024 + kData + kCtrl;
+    static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
+    static_assert(kWBytes % 1024 == 0 && kBBytes % 1024 == 0, "stage alignment");
+    static_assert(kSmem <= 232448, "shared memory budget");
+    static_assert(BN % 16 == 0 && BN <= 256, "token tile");
+};
+
+struct TileInfo {
+    int e, rt, tt, ks, tok0, ntok;
+};
+
+__device__ __forceinline__ TileInfo decode_tile(int t, const int* s_cnt, const int* s_off,
+                                                const int* s_pre, int E, int BN, int ksplit)
+{
+    TileInfo ti;
+    int e = 0;
+    while (e + 1 < E && s_pre[e + 1] <= t)
+        ++e;
+    const int local = t - s_pre[e];
+    const int c = s_cnt[e];
+    const int ntt = (c + BN - 1) / BN;
+    const int per_rt = ntt * ksplit;
+    ti.e = e;
+    ti.rt = local / per_rt;
+    const int r2 = local - ti.rt * per_rt;
+    ti.tt = r2 / ksplit;
+    ti.ks = r2 - ti.tt * ksplit;
+    ti.tok0 = s_off[e] + ti.tt * BN;
+    ti.ntok = min(BN, c - ti.tt * BN);
+    return ti;
+}
+
+// Nibbles -> E4M3 operand bytes worth (q + 8) * 2^-9, in K order.
+__device__ __forceinline__ void unpack8(uint32_t w, uint32_t& lo4, uint32_t& hi4)
+{
+    const uint32_t ev = (w & 0x0F0F0F0Fu) ^ 0x08080808u;         // codes 0,2,4,6
+    const uint32_t od = ((w >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;  // codes 1,3,5,7
+    lo4 = prmt(ev, od, 0x5140u);                                 // 0,1,2,3
+    hi4 = prmt(ev, od, 0x7362u);                                 // 4,5,6,7
+}
+
+__device__ __forceinline__ float act_fn(float g, int act)
+{
+    if (act == 0)
+        return __fdiv_rn(g, 1.0f + expf(-g));
+    const float c = 0.7978845608028654f;  // sqrt(2/pi)
+    return 0.5f * g * (1.0f + tanhf(c * (g + 0.044715f * g * g * g)));
+}
+
+template <int MODE, int BN, int KC, int PST, int AST>
+__global__ void __launch_bounds__(384, 1)
+    moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b,
+                    const MoeGemmParams p)
+{
+    using Tr = MoeTraits<MODE, BN, KC, PST, AST>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    uint8_t* pring = smem;
+    uint8_t* aring = smem + PST * Tr::kPBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(aring + AST * Tr::kABytes);
+    uint64_t* full = bars;
+    uint64_t* empty = full + PST;
+    uint64_t* afull = empty + PST;
+    uint64_t* aempty = afull + AST;
+    uint64_t* accfull = aempty + AST;
+    uint64_t* accempty = accfull + 2;
+    uint64_t* drain = accempty + 2;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+    int* s_cnt = reinterpret_cast<int*>(s_tmem + 4);
+    int* s_off = s_cnt + 256;
+    int* s_pre = s_off + 260;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < PST; ++i) {
+            mbar_init(smem_u32(&full[i]), 1);
+            mbar_init(smem_u32(&empty[i]), 4 + 1);
+        }
+        for (int i = 0; i < AST; ++i) {
+            mbar_init(smem_u32(&afull[i]), 4);
+            mbar_init(smem_u32(&aempty[i]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&accfull[i]), 1);
+            mbar_init(smem_u32(&accempty[i]), 4);
+        }
+        mbar_init(smem_u32(drain), 1);
+        fence_mbar_init();
+        *s_abort = 0;
+    }
+    if (threadIdx.x == 64) {
+        int acc = 0;
+        for (int e = 0; e < p.E; ++e) {
+            const int c = p.counts[e];
+            s_cnt[e] = c;
+            s_off[e] = p.offsets[e];
+            s_pre[e] = acc;
+            acc += p.rt_count * ((c + BN - 1) / BN) * p.ksplit;
+        }
+        s_pre[p.E] = acc;
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tm_w);
+        prefetch_tmap(&tm_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(s_tmem), Tr::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+    const int total = s_pre[p.E];
+
+    auto fail = [&]() {
+        *s_abort = 1;
+        set_error(p.err, kErrBitTimeout);
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first();
+            const uint64_t pol_b = policy_evict_last();
+            int ps = 0;
+            uint32_t ph = 0;
+            uint32_t issued = 0;       // bit s: stage s was filled at least once
+            uint32_t last_par = 0;     // bit s: parity of the last fill of stage s
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                const TileInfo ti = decode_tile(t, s_cnt, s_off, s_pre, p.E, BN, p.ksplit);
+                for (int kb = 0; kb < p.kblocks; ++kb) {
+                    if (*s_abort || !mbar_wait(smem_u32(&empty[ps]), ph ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&full[ps]);
+                    mbar_arrive_expect_tx(fb, Tr::kPBytes);
+                    uint8_t* st = pring + ps * Tr::kPBytes;
+                    const int kel = (ti.ks * p.kblocks + kb) * KC;  // first K element
+                    if (MODE == 0) {
+                        const int r0 = ti.e * p.rows_per_expert + ti.rt * 64;
+                        tma_load_2d_hint(smem_u32(st), &tm_w, kel / 2, r0, fb, pol_w);
+                        tma_load_2d_hint(smem_u32(st + Tr::kWBytes / 2), &tm_w, kel / 2, r0 + p.I, fb,
+                                         pol_w);
+                    } else {
+                        const int r0 = ti.e * p.rows_per_expert + ti.rt * 128;
+                        tma_load_2d_hint(smem_u32(st), &tm_w, kel / 2, r0, fb, pol_w);
+                    }
+#pragma unroll
+                    for (int a = 0; a < Tr::kAtoms; ++a)
+                        tma_load_2d_hint(smem_u32(st + Tr::kWBytes + a * BN * 128), &tm_b,
+                                         kel + a * 128, ti.tok0, fb, pol_b);
+                    issued |= 1u << ps;
+                    last_par = (last_par & ~(1u << ps)) | (ph << ps);
+                    if (++ps == PST) {
+                        ps = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                fail();
+                // let every issued copy land before the CTA's shared memory goes away
+                for (int s = 0; s < PST; ++s)
+                    if ((issued >> s) & 1u)
+                        mbar_wait(smem_u32(&full[s]), (last_par >> s) & 1u);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int ps = 0, as = 0;
+            uint32_t pph = 0, aph = 0;
+            int it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
+                const TileInfo ti = decode_tile(t, s_cnt, s_off, s_pre, p.E, BN, p.ksplit);
+                const int nmma = max(16, (ti.ntok + 15) & ~15);
+                const uint32_t idesc = idesc_e4m3_f32(128, nmma);
+                const int d = it & 1;
+                const uint32_t use = static_cast<uint32_t>(it >> 1);
+                if (*s_abort || !mbar_wait(smem_u32(&accempty[d]), (use & 1u) ^ 1u)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t dt = tmem + static_cast<uint32_t>(d * BN);
+                for (int kb = 0; kb < p.kblocks; ++kb) {
+                    if (*s_abort || !mbar_wait(smem_u32(&full[ps]), pph) ||
+                        !mbar_wait(smem_u32(&afull[as]), aph)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t abase = smem_u32(aring + as * Tr::kABytes);
+                    const uint32_t bbase = smem_u32(pring + ps * Tr::kPBytes + Tr::kWBytes);
+#pragma unroll
+                    for (int kk = 0; kk < KC / 32; ++kk) {
+                        const int atom = kk >> 2, sub = kk & 3;
+                        const uint64_t ad = desc_kmajor_sw128(abase + atom * (128 * 128) + sub * 32);
+                        const uint64_t bd = desc_kmajor_sw128(bbase + atom * (BN * 128) + sub * 32);
+                        umma_f8(dt, ad, bd, idesc, (kb | kk) ? 1u : 0u);
+                    }
+                    umma_commit(smem_u32(&empty[ps]));
+                    umma_commit(smem_u32(&aempty[as]));
+                    if (++ps == PST) {
+                        ps = 0;
+                        pph ^= 1u;
+                    }
+                    if (++as == AST) {
+                        as = 0;
+                        aph ^= 1u;
+                    }
+                }
+                if (!ok)
+                    break;
+                umma_commit(smem_u32(&accfull[d]));
+            }
+            if (!ok) {
+                fail();
+                umma_commit(smem_u32(drain));  // wait for MMAs in flight before TMEM goes away
+                mbar_wait(smem_u32(drain), 0);
+            }
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ------------------------------------------------------------ converters
+        const int r = threadIdx.x - 128;  // A row == TMEM lane
+        int src = r;
+        if (MODE == 0) {
+            // lanes 0-15 of each 32-lane quadrant: gate rows; lanes 16-31: the
+            // matching up rows (so one warp holds both halves of a gated pair)
+            const int q = r >> 5, j = r & 31;
+            src = (j < 16) ? (16 * q + j) : (64 + 16 * q + (j - 16));
+        }
+        int ps = 0, as = 0;
+        uint32_t pph = 0, aph = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            for (int kb = 0; kb < p.kblocks; ++kb) {
+                if (*s_abort || !mbar_wait(smem_u32(&full[ps]), pph) ||
+                    !mbar_wait(smem_u32(&aempty[as]), aph ^ 1u)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t* wrow = pring + ps * Tr::kPBytes + src * (KC / 2);
+                uint8_t* abase = aring + as * Tr::kABytes + r * 128;
+#pragma unroll
+                for (int c = 0; c < KC / 32; ++c) {
+                    // packed 16-byte chunk c of this row, after the TMA swizzle
+                    const int pc = (KC == 256) ? (c ^ (src & 7)) : (c ^ ((src >> 1) & 3));
+                    const uint4 w4 = *reinterpret_cast<const uint4*>(wrow + pc * 16);
+                    uint4 o0, o1;
+                    unpack8(w4.x, o0.x, o0.y);
+                    unpack8(w4.y, o0.z, o0.w);
+                    unpack8(w4.z, o1.x, o1.y);
+                    unpack8(w4.w, o1.z, o1.w);
+                    const int atom = (32 * c) >> 7;
+                    const int c16 = ((32 * c) & 127) >> 4;
+                    uint8_t* arow = abase + atom * (128 * 128);
+                    *reinterpret_cast<uint4*>(arow + ((c16 ^ (r & 7)) << 4)) = o0;
+                    *reinterpret_cast<uint4*>(arow + (((c16 + 1) ^ (r & 7)) << 4)) = o1;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(smem_u32(&afull[as]));
+                    mbar_arrive(smem_u32(&empty[ps]));
+                }
+                if (++ps == PST) {
+                    ps = 0;
+                    pph ^= 1u;
+                }
+                if (++as == AST) {
+                    as = 0;
+                    aph ^= 1u;
+                }
+            }
+        }
+        if (!ok)
+            fail();
+    } else if (warp >= 8) {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;
+        const float a1 = __ldg(p.a1);
+        const float a2 = __ldg(p.a2);
+        int it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
+            const TileInfo ti = decode_tile(t, s_cnt, s_off, s_pre, p.E, BN, p.ksplit);
+            const int d = it & 1;
+            const uint32_t use = static_cast<uint32_t>(it >> 1);
+            if (*s_abort || !mbar_wait(smem_u32(&accfull[d]), use & 1u)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>(d * BN);
+            const int nchunks = (ti.ntok + 31) >> 5;
+            if (MODE == 0) {
+                const int half = lane >> 4;  // 0: gate lane, 1: up lane
+                const int i = ti.rt * 64 + 16 * q + (lane & 15);
+                const float sg = a1 * __ldg(p.s_gu + static_cast<int64_t>(ti.e) * 2 * p.I + i);
+                const float su = a1 * __ldg(p.s_gu + static_cast<int64_t>(ti.e) * 2 * p.I + p.I + i);
+                for (int ch = 0; ch < nchunks; ++ch) {
+                    uint32_t v[32];
+                    tmem_ld32(tbase + ch * 32, v);
+                    tmem_ld_wait();
+                    int s512[16];
+#pragma unroll
+                    for (int cc = 0; cc < 16; ++cc) {
+                        // gate lanes finish column cc, up lanes column 16+cc
+                        const float send = __uint_as_float(half ? v[cc] : v[cc + 16]);
+                        const float recv = __shfl_xor_sync(0xFFFFFFFFu, send, 16);
+                        const float pg = half ? recv : __uint_as_float(v[cc]);
+                        const float pu = half ? __uint_as_float(v[cc + 16]) : recv;
+                        const int col = ch * 32 + cc + 16 * half;
+                        s512[cc] = 0;
+                        if (col < ti.ntok) {
+                            const int pos = ti.tok0 + col;
+                            const float shift = static_cast<float>(p.s0x[pos]) * (1.0f / 64.0f);
+                            const float G = fmaf(512.0f, pg, -shift);
+                            const float U = fmaf(512.0f, pu, -shift);
+                            const float h = act_fn(sg * G, p.act) * (su * U);
+                            const uint32_t code = cvt_e4m3(__fdiv_rn(h, a2));
+                            p.hq[static_cast<int64_t>(pos) * p.I + i] = static_cast<uint8_t>(code);
+                            s512[cc] = e4m3_times512(code);
+                        }
+                    }
+                    // reduce-scatter over the 16 lanes of each half: lane ends
+                    // with the sum of column ch*32 + lane over this warp's rows
+#pragma unroll
+                    for (int m = 8; m >= 1; m >>= 1) {
+                        const bool upper = (lane & m) != 0;
+#pragma unroll
+                        for (int x = 0; x < m; ++x) {
+                            const int send = upper ? s512[x] : s512[x + m];
+                            const int recv = __shfl_xor_sync(0xFFFFFFFFu, send, m);
+                            s512[x] = (upper ? s512[x + m] : s512[x]) + recv;
+                        }
+                    }
+                    const int col = ch * 32 + lane;
+                    if (col < ti.ntok && s512[0] != 0)
+                        atomicAdd(p.s0h + ti.tok0 + col,
+                                  static_cast<unsigned long long>(static_cast<long long>(s512[0])));
+                }
+            } else {
+                const int n = ti.rt * 128 + q * 32 + lane;
+                float* yb = p.ypart + (static_cast<int64_t>(ti.ks) * p.A + ti.tok0) * p.H + n;
+                for (int ch = 0; ch < nchunks; ++ch) {
+                    uint32_t v[32];
+                    tmem_ld32(tbase + ch * 32, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int cc = 0; cc < 32; ++cc) {
+                        const int col = ch * 32 + cc;
+                        if (col < ti.ntok)
+                            yb[static_cast<int64_t>(col) * p.H] = __uint_as_float(v[cc]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_u32(&accempty[d]));
+        }
+        if (!ok)
+            fail();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, Tr::kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Gather: xp[pos] = x[sorted[pos] / k]; s0x[pos] = sum_h 512*dec(x) (exact);
+// s0h[pos] = 0 (the gate_up epilogue accumulates into it).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) moe_gather_kernel(const uint8_t* __restrict__ xq, int H, int k,
+                                                         const int32_t* __restrict__ sorted_ids,
+                                                         int A, uint8_t* __restrict__ xp,
+                                                         long long* __restrict__ s0x,
+                                                         unsigned long long* __restrict__ s0h)
+{
+    const int lane = threadIdx.x & 31;
+    const int pos = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (pos >= A)
+        return;
+    const int t = __ldg(sorted_ids + pos) / k;
+    const uint4* src = reinterpret_cast<const uint4*>(xq + static_cast<int64_t>(t) * H);
+    uint4* dst = reinterpret_cast<uint4*>(xp + static_cast<int64_t>(pos) * H);
+    long long sum = 0;
+    for (int c = lane; c < H / 16; c += 32) {
+        const uint4 v = __ldg(src + c);
+        dst[c] = v;
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+        int s = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+                s += e4m3_times512((u[j] >> (8 * b)) & 0xFFu);
+        sum += s;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+    if (lane == 0) {
+        s0x[pos] = sum;
+        s0h[pos] = 0ull;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Combine: out[t, n] = bf16( sum_j w[t,j] * a2 * S_d[e,n] * D ),
+// D = 512 * sum_splits P - s0h/64, in j then split order (deterministic).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) moe_finalize_kernel(
+    int T, int H, int k, int A, int ksplit, const int32_t* __restrict__ ids,
+    const float* __restrict__ topk_w, const int32_t* __restrict__ inv,
+    const float* __restrict__ ypart, const unsigned long long* __restrict__ s0h,
+    const float* __restrict__ s_d, const float* __restrict__ a2p, uint16_t* __restrict__ out)
+{
+    const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int per_row = H / 4;
+    if (idx >= static_cast<int64_t>(T) * per_row)
+        return;
+    const int t = static_cast<int>(idx / per_row);
+    const int n = static_cast<int>(idx % per_row) * 4;
+    const float a2 = __ldg(a2p);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < k; ++j) {
+        const int a = t * k + j;
+        const int pos = __ldg(inv + a);
+        const int e = __ldg(ids + a);
+        const float wt = __ldg(topk_w + a);
+        float4 P = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s = 0; s < ksplit; ++s) {
+            const float4 v =
+                __ldg(reinterpret_cast<const float4*>(ypart + (static_cast<int64_t>(s) * A + pos) * H + n));
+            P.x += v.x;
+            P.y += v.y;
+            P.z += v.z;
+            P.w += v.w;
+        }
+        const float shift = static_cast<float>(static_cast<long long>(__ldg(s0h + pos))) * (1.0f / 64.0f);
+        const float4 sd = __ldg(reinterpret_cast<const float4*>(s_d + static_cast<int64_t>(e) * H + n));
+        const float Pv[4] = {P.x, P.y, P.z, P.w};
+        const float Sv[4] = {sd.x, sd.y, sd.z, sd.w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const float D = fmaf(512.0f, Pv[c], -shift);
+            acc[c] = fmaf(wt, a2 * Sv[c] * D, acc[c]);
+        }
+    }
+    uint2 o;
+    o.x = static_cast<uint32_t>(float_to_bf16_bits(acc[0])) |
+          (static_cast<uint32_t>(float_to_bf16_bits(acc[1])) << 16);
+    o.y = static_cast<uint32_t>(float_to_bf16_bits(acc[2])) |
+          (static_cast<uint32_t>(float_to_bf16_bits(acc[3])) << 16);
+    *reinterpret_cast<uint2*>(out + static_cast<int64_t>(t) * H + n) = o;
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+int moe_ksplit_max(int T, int k)
+{
+    const int64_t A = static_cast<int64_t>(T) * k;
+    if (A <= 128)
+        return 16;
+    if (A <= 1024)
+        return 4;
+    return 1;
+}
+
+static int pick_bn(int T)
+{
+    if (T <= 32)
+        return 32;
+    if (T <= 64)
+        return 64;
+    if (T <= 128)
+        return 128;
+    return 256;
+}
+
+MoeConfig moe_pick_config(int T, int H, int I, int E, int k, int num_sms)
+{
+    MoeConfig c;
+    c.bn = pick_bn(T);
+    c.kc = (c.bn <= 64) ? 256 : 128;
+    // split the down projection's K so that its tiles fill the SMs evenly
+    const int kblocks = I / c.kc;
+    const int base_tiles = E * (H / 128);
+    const int kmax = moe_ksplit_max(T, k);
+    int best = 1;
+    double best_eff = 0.0;
+    for (int d = 1; d <= kmax; ++d) {
+        if (kblocks % d != 0 || kblocks / d < 2)
+            continue;
+        const int64_t tiles = static_cast<int64_t>(base_tiles) * d;
+        const int64_t waves = (tiles + num_sms - 1) / num_sms;
+        const double eff = static_cast<double>(tiles) / static_cast<double>(waves * num_sms);
+        if (eff > best_eff + 0.02) {
+            best_eff = eff;
+            best = d;
+        }
+    }
+    c.ksplit = best;
+    return c;
+}
+
+template <int MODE, int BN, int KC, int PST, int AST>
+static int launch_gemm(const CUtensorMap& tw, const CUtensorMap& tb, const MoeGemmParams& prm, int grid,
+                       cudaStream_t s)
+{
+    using Tr = MoeTraits<MODE, BN, KC, PST, AST>;
+    auto kern = moe_gemm_kernel<MODE, BN, KC, PST, AST>;
+    // attribute set on every launch: cheap, and correct for every device
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Tr::kSmem) != cudaSuccess)
+        return kErrLaunch;
+    kern<<<grid, 384, Tr::kSmem, s>>>(tw, tb, prm);
+    return cudaGetLastError() == cudaSuccess ? kOK : kErrLaunch;
+}
+
+template <int MODE>
+static int dispatch_gemm(const MoeConfig& cfg, const CUtensorMap& tw, const CUtensorMap& tb,
+                         const MoeGemmParams& prm, int grid, cudaStream_t s)
+{
+    switch (cfg.bn) {
+    case 32: return launch_gemm<MODE, 32, 256, 6, 2>(tw, tb, prm, grid, s);
+    case 64: return launch_gemm<MODE, 64, 256, 4, 2>(tw, tb, prm, grid, s);
+    case 128: return launch_gemm<MODE, 128, 128, 6, 2>(tw, tb, prm, grid, s);
+    default: return launch_gemm<MODE, 256, 128, 4, 2>(tw, tb, prm, grid, s);
+    }
+}
+
+int launch_moe_forward(const MoeLaunch& L, const MoeConfig& cfg, int num_sms, cudaStream_t s)
+{
+    const int A = L.T * L.k;
+    const int BN = cfg.bn, KC = cfg.kc;
+    // activations: gather + exact per-token sums
+    moe_gather_kernel<<<(A + 7) / 8, 256, 0, s>>>(L.xq, L.H, L.k, L.sorted_ids, A, L.xp, L.s0x, L.s0h);
+    if (cudaGetLastError() != cudaSuccess)
+        return kErrLaunch;
+
+    const CUtensorMapSwizzle wsw = (KC == 256) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    CUtensorMap tw_gu, tb_gu, tw_d, tb_d;
+    if (!encode_map_2d(&tw_gu, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.w_gu, L.H / 2,
+                       static_cast<uint64_t>(L.E) * 2 * L.I, L.H / 2, KC / 2, 64, wsw) ||
+        !encode_map_2d(&tb_gu, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.xp, L.H, A, L.H, 128, BN,
+                       CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_map_2d(&tw_d, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.w_d, L.I / 2,
+                       static_cast<uint64_t>(L.E) * L.H, L.I / 2, KC / 2, 128, wsw) ||
+        !encode_map_2d(&tb_d, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.hq, L.I, A, L.I, 128, BN,
+                       CU_TENSOR_MAP_SWIZZLE_128B))
+        return kErrLaunch;
+
+    const int64_t tok_tiles_max = (A + BN - 1) / BN + L.E;
+    MoeGemmParams g{};
+    g.counts = L.counts;
+    g.offsets = L.offsets;
+    g.E = L.E;
+    g.I = L.I;
+    g.H = L.H;
+    g.A = A;
+    g.s_gu = L.s_gu;
+    g.a1 = L.a1;
+    g.a2 = L.a2;
+    g.act = L.act;
+    g.s0x = L.s0x;
+    g.hq = L.hq;
+    g.s0h = L.s0h;
+    g.ypart = L.ypart;
+    g.err = L.err;
+
+    auto mark = [&](int i) {
+        if (L.events[i])
+            cudaEventRecord(static_cast<cudaEvent_t>(L.events[i]), s);
+    };
+    // gate_up: 64 gated pairs (128 weight rows) per tile, full K = H
+    mark(0);
+    MoeGemmParams gu = g;
+    gu.rows_per_expert = 2 * L.I;
+    gu.rt_count = L.I / 64;
+    gu.kblocks = L.H / KC;
+    gu.ksplit = 1;
+    int64_t tiles = static_cast<int64_t>(gu.rt_count) * tok_tiles_max;
+    int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
+    int st = dispatch_gemm<0>(cfg, tw_gu, tb_gu, gu, grid, s);
+    if (st != kOK)
+        return st;
+    mark(1);
+
+    // down: 128 output rows per tile, K = I split ksplit ways
+    MoeGemmParams dn = g;
+    dn.rows_per_expert = L.H;
+    dn.rt_count = L.H / 128;
+    dn.ksplit = cfg.ksplit;
+    dn.kblocks = L.I / KC / cfg.ksplit;
+    tiles = static_cast<int64_t>(dn.rt_count) * tok_tiles_max * cfg.ksplit;
+    grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
+    st = dispatch_gemm<1>(cfg, tw_d, tb_d, dn, grid, s);
+    if (st != kOK)
+        return st;
+    mark(2);
+
+    const int64_t nthreads = static_cast<int64_t>(L.T) * (L.H / 4);
+    moe_finalize_kernel<<<static_cast<unsigned>((nthreads + 255) / 256), 256, 0, s>>>(
+        L.T, L.H, L.k, A, cfg.ksplit, L.ids, L.topk_w, L.inv, L.ypart, L.s0h, L.s_d, L.a2, L.out);
+    if (cudaGetLastError() != cudaSuccess)
+        return kErrLaunch;
+    mark(3);
+    return kOK;
+}
+
+}  // namespace w4a8

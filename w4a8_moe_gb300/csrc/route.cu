@@ -1,0 +1,284 @@
+// Router: softmax top-k with renormalized weights, per-expert histogram and a
+// stable permutation of the T*k assignments grouped by expert.
+//
+// "ROCm: enable trillion-parameter MoE models with INT4-FP8 single node",
+// config.json: num_local_experts, num_experts_per_tok, and ignored_layers (the
+// block_sparse_moe.gate stays unquantized, so routing runs on fp32 logits).
+//
+// Selection ranks the fp32 logits (softmax is monotone), descending, equal
+// logits by lower expert index. Weights: with renormalization
+// w_j = exp(l_j - m) / sum_{j' selected} exp(l_j' - m), which equals the
+// renormalized softmax probabilities; without it, the softmax over all E.
+// Permutation: counting sort that keeps assignment order a = t*k + j within
+// each expert, so the result is unique and compared bit-exactly.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace w4a8 {
+
+constexpr int kMaxE = 256;
+
+// One warp per token; lane l holds logits l, l+32, ... (E <= 256).
+__device__ __forceinline__ void route_token(const float* __restrict__ logits, int t, int E, int k,
+                                            int renorm, int32_t* __restrict__ ids,
+                                            float* __restrict__ w, int32_t* s_ids)
+{
+    const int lane = threadIdx.x & 31;
+    float v[kMaxE / 32];
+#pragma unroll
+    for (int i = 0; i < kMaxE / 32; ++i) {
+        const int e = lane + 32 * i;
+        v[i] = (e < E) ? __ldg(logits + static_cast<int64_t>(t) * E + e) : -INFINITY;
+    }
+    uint32_t taken = 0;  // bit i: entry lane + 32 i already selected
+    float mx = -INFINITY;
+    float sel_sum = 0.0f;
+    float sel_val[8];
+    for (int j = 0; j < k; ++j) {
+        // best among this lane's untaken entries: larger value, then lower index
+        float bv = -INFINITY;
+        int be = 0x7FFFFFFF;
+#pragma unroll
+        for (int i = 0; i < kMaxE / 32; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E && !((taken >> i) & 1u) && (be == 0x7FFFFFFF || v[i] > bv)) {
+                bv = v[i];
+                be = e;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
+            const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, o);
+            if (oe != 0x7FFFFFFF && (be == 0x7FFFFFFF || ov > bv || (ov == bv && oe < be))) {
+                bv = ov;
+                be = oe;
+            }
+        }
+        if ((be & 31) == lane)
+            taken |= 1u << (be >> 5);
+        if (j == 0)
+            mx = bv;
+        if (j < 8)
+            sel_val[j] = bv;
+        const float p = expf(bv - mx);
+        sel_sum += p;
+        if (lane == 0) {
+            ids[static_cast<int64_t>(t) * k + j] = be;
+            if (s_ids)
+                s_ids[t * k + j] = be;
+        }
+    }
+    float denom = sel_sum;
+    if (!renorm) {
+        float sum = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kMaxE / 32; ++i)
+            if (lane + 32 * i < E)
+                sum += expf(v[i] - mx);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+        denom = sum;
+    }
+    if (lane == 0) {
+        for (int j = 0; j < k; ++j) {
+            float lv;
+            if (j < 8) {
+                lv = sel_val[j];
+            } else {
+                lv = __ldg(logits + static_cast<int64_t>(t) * E + ids[static_cast<int64_t>(t) * k + j]);
+            }
+            w[static_cast<int64_t>(t) * k + j] = __fdiv_rn(expf(lv - mx), denom);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T,
+                                                         int E, int k, int renorm,
+                                                         int32_t* __restrict__ ids,
+                                                         float* __restrict__ w)
+{
+    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (t < T)
+        route_token(logits, t, E, k, renorm, ids, w, nullptr);
+}
+
+// Per-chunk expert histogram: block b counts assignments [b*C, (b+1)*C).
+__global__ void __launch_bounds__(256) route_hist_kernel(const int32_t* __restrict__ ids, int A,
+                                                         int E, int32_t* __restrict__ block_hist)
+{
+    __shared__ int cnt[kMaxE];
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        cnt[e] = 0;
+    __syncthreads();
+    const int a0 = blockIdx.x * kRouteChunk;
+    const int a1 = min(A, a0 + kRouteChunk);
+    for (int a = a0 + threadIdx.x; a < a1; a += blockDim.x)
+        atomicAdd(&cnt[__ldg(ids + a)], 1);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        block_hist[static_cast<int64_t>(blockIdx.x) * E + e] = cnt[e];
+}
+
+// Exclusive scan in (expert, block) order: base[b][e] = offsets[e] + sum of
+// block_hist[b'][e] for b' < b. One block.
+__global__ void __launch_bounds__(256) route_scan_kernel(const int32_t* __restrict__ block_hist,
+                                                         int nb, int E, int A,
+                                                         int32_t* __restrict__ counts,
+                                                         int32_t* __restrict__ offsets,
+                                                         int32_t* __restrict__ block_base)
+{
+    __shared__ int tot[kMaxE];
+    __shared__ int off[kMaxE + 1];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int s = 0;
+        for (int b = 0; b < nb; ++b)
+            s += block_hist[static_cast<int64_t>(b) * E + e];
+        tot[e] = s;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int run = 0;
+        for (int e = 0; e < E; ++e) {
+            off[e] = run;
+            run += tot[e];
+        }
+        off[E] = run;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        counts[e] = tot[e];
+        offsets[e] = off[e];
+        int run = off[e];
+        for (int b = 0; b < nb; ++b) {
+            block_base[static_cast<int64_t>(b) * E + e] = run;
+            run += block_hist[static_cast<int64_t>(b) * E + e];
+        }
+    }
+    if (threadIdx.x == 0)
+        offsets[E] = A;
+}
+
+// Stable scatter of one chunk of assignments. Rounds of blockDim.x
+// assignments in order; inside a round a warp ranks equal experts with
+// match.any, warps are ordered through per-warp counts in shared memory, and
+// `run` carries the per-expert count of earlier rounds.
+template <int NW>
+__device__ __forceinline__ void scatter_chunk(const int32_t* ids, int a0, int a1, int E,
+                                              const int32_t* base, int* run, int (*wcnt)[kMaxE],
+                                              int32_t* __restrict__ sorted_ids,
+                                              int32_t* __restrict__ inv)
+{
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    for (int r0 = a0; r0 < a1; r0 += NW * 32) {
+        for (int e = lane; e < E; e += 32)
+            wcnt[wid][e] = 0;
+        __syncwarp();
+        const int a = r0 + threadIdx.x;
+        const bool valid = a < a1;
+        const int e = valid ? ids[a] : -1;
+        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, e);
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        if (valid && rank == 0)
+            wcnt[wid][e] = __popc(peers);
+        __syncthreads();
+        if (valid) {
+            int before = 0;
+            for (int w2 = 0; w2 < wid; ++w2)
+                before += wcnt[w2][e];
+            const int pos = base[e] + run[e] + before + rank;
+            sorted_ids[pos] = a;
+            inv[a] = pos;
+        }
+        __syncthreads();
+        for (int e2 = threadIdx.x; e2 < E; e2 += blockDim.x) {
+            int s = 0;
+            for (int w2 = 0; w2 < NW; ++w2)
+                s += wcnt[w2][e2];
+            run[e2] += s;
+        }
+        __syncthreads();
+    }
+}
+
+__global__ void __launch_bounds__(256) route_scatter_kernel(const int32_t* __restrict__ ids, int A,
+                                                            int E,
+                                                            const int32_t* __restrict__ block_base,
+                                                            int32_t* __restrict__ sorted_ids,
+                                                            int32_t* __restrict__ inv)
+{
+    __shared__ int run[kMaxE];
+    __shared__ int base[kMaxE];
+    __shared__ int wcnt[8][kMaxE];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        run[e] = 0;
+        base[e] = block_base[static_cast<int64_t>(blockIdx.x) * E + e];
+    }
+    __syncthreads();
+    const int a0 = blockIdx.x * kRouteChunk;
+    const int a1 = min(A, a0 + kRouteChunk);
+    scatter_chunk<8>(ids, a0, a1, E, base, run, wcnt, sorted_ids, inv);
+}
+
+// Small problems (T*k <= kRouteFusedMax): one block of 512 threads does
+// top-k, histogram, scan and scatter.
+__global__ void __launch_bounds__(512) route_fused_kernel(const float* __restrict__ logits, int T,
+                                                           int E, int k, int renorm,
+                                                           int32_t* __restrict__ ids,
+                                                           float* __restrict__ w,
+                                                           int32_t* __restrict__ counts,
+                                                           int32_t* __restrict__ offsets,
+                                                           int32_t* __restrict__ sorted_ids,
+                                                           int32_t* __restrict__ inv)
+{
+    __shared__ int32_t s_ids[kRouteFusedMax];
+    __shared__ int cnt[kMaxE];
+    __shared__ int base[kMaxE];
+    __shared__ int wcnt[16][kMaxE];
+    const int A = T * k;
+    const int wid = threadIdx.x >> 5;
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        cnt[e] = 0;
+    for (int t = wid; t < T; t += 16)
+        route_token(logits, t, E, k, renorm, ids, w, s_ids);
+    __syncthreads();
+    for (int a = threadIdx.x; a < A; a += blockDim.x)
+        atomicAdd(&cnt[s_ids[a]], 1);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int run = 0;
+        for (int e = 0; e < E; ++e) {
+            base[e] = run;
+            offsets[e] = run;
+            counts[e] = cnt[e];
+            run += cnt[e];
+        }
+        offsets[E] = run;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        cnt[e] = 0;  // reused as the running count
+    __syncthreads();
+    scatter_chunk<16>(s_ids, 0, A, E, base, cnt, wcnt, sorted_ids, inv);
+}
+
+cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, int32_t* ids,
+                         float* w, int32_t* counts, int32_t* offsets, int32_t* sorted_ids,
+                         int32_t* inv, int32_t* block_hist, int32_t* block_base, cudaStream_t s)
+{
+    const int A = T * k;
+    if (A <= kRouteFusedMax) {
+        route_fused_kernel<<<1, 512, 0, s>>>(logits, T, E, k, renorm, ids, w, counts, offsets,
+                                              sorted_ids, inv);
+        return cudaGetLastError();
+    }
+    const int nb = (A + kRouteChunk - 1) / kRouteChunk;
+    route_topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(logits, T, E, k, renorm, ids, w);
+    route_hist_kernel<<<nb, 256, 0, s>>>(ids, A, E, block_hist);
+    route_scan_kernel<<<1, 256, 0, s>>>(block_hist, nb, E, A, counts, offsets, block_base);
+    route_scatter_kernel<<<nb, 256, 0, s>>>(ids, A, E, block_base, sorted_ids, inv);
+    return cudaGetLastError();
+}
+
+}  // namespace w4a8

@@ -15,8 +15,9 @@ description) plus an o_proj-shaped [2560,6144].
 
 Distributions: weights N(0, 0.02) rounded to bf16; activations N(0, 1) in bf16;
 router logits N(0, 1) in fp32, plus an optional per-expert logit bias that
-skews the expert load. One generator per call, drawn in a fixed order
-(logits, bias, x, gate_up, down).
+skews the expert load. Each tensor kind has its own generator seeded with
+seed * 16 + a fixed offset (logits 1, bias 2, x 3, gate_up 4, down 5), so the
+weights of a layer do not depend on the number of tokens drawn with them.
 """
 from __future__ import annotations
 
@@ -55,39 +56,44 @@ BLOCK_FP8_SHAPES = [(16384, 2560), (13312, 2560), (2560, 6144)]
 BLOCK_FP8_M = [1, 8, 64, 4096]
 
 
-def _gen(seed: int, device) -> torch.Generator:
+def _gen(seed: int, device, offset: int) -> torch.Generator:
     g = torch.Generator(device=device)
-    g.manual_seed(seed)
+    g.manual_seed(seed * 16 + offset)
     return g
 
 
 def moe_inputs(T: int, H: int, I: int, E: int, bias_std: float = 0.0, seed: int = 0,
                device="cpu", weights: bool = True, weight_std: float = 0.02):
     """Router logits fp32 [T,E] (bias added), x bf16 [T,H], W_gu bf16 [E,2I,H], W_d bf16 [E,H,I]."""
-    g = _gen(seed, device)
-    logits = torch.randn(T, E, generator=g, device=device, dtype=torch.float32)
-    bias = torch.randn(E, generator=g, device=device, dtype=torch.float32) * bias_std
+    logits = torch.randn(T, E, generator=_gen(seed, device, 1), device=device, dtype=torch.float32)
     if bias_std:
-        logits = logits + bias
-    x = torch.randn(T, H, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+        bias = torch.randn(E, generator=_gen(seed, device, 2), device=device, dtype=torch.float32)
+        logits = logits + bias * bias_std
+    x = torch.randn(T, H, generator=_gen(seed, device, 3), device=device,
+                    dtype=torch.float32).to(torch.bfloat16)
     out = {"logits": logits.contiguous(), "x": x.contiguous()}
     if weights:
-        w_gu = torch.empty(E, 2 * I, H, device=device, dtype=torch.bfloat16)
-        w_d = torch.empty(E, H, I, device=device, dtype=torch.bfloat16)
-        for e in range(E):  # per expert keeps the fp32 temporary small
-            w_gu[e] = (torch.randn(2 * I, H, generator=g, device=device) * weight_std).to(torch.bfloat16)
-        for e in range(E):
-            w_d[e] = (torch.randn(H, I, generator=g, device=device) * weight_std).to(torch.bfloat16)
-        out["w_gu"] = w_gu
-        out["w_d"] = w_d
+        out.update(moe_weights(H, I, E, seed=seed, device=device, weight_std=weight_std))
     return out
+
+
+def moe_weights(H: int, I: int, E: int, seed: int = 0, device="cpu", weight_std: float = 0.02):
+    """W_gu bf16 [E,2I,H] (rows [0,I) gate, [I,2I) up) and W_d bf16 [E,H,I]."""
+    g_gu = _gen(seed, device, 4)
+    g_d = _gen(seed, device, 5)
+    w_gu = torch.empty(E, 2 * I, H, device=device, dtype=torch.bfloat16)
+    w_d = torch.empty(E, H, I, device=device, dtype=torch.bfloat16)
+    for e in range(E):  # per expert keeps the fp32 temporary small
+        w_gu[e] = (torch.randn(2 * I, H, generator=g_gu, device=device) * weight_std).to(torch.bfloat16)
+    for e in range(E):
+        w_d[e] = (torch.randn(H, I, generator=g_d, device=device) * weight_std).to(torch.bfloat16)
+    return {"w_gu": w_gu, "w_d": w_d}
 
 
 def block_fp8_inputs(M: int, N: int, K: int, seed: int = 0, device="cpu", weight_std: float = 0.02):
     """Activations x bf16 [M,K] and a dense weight bf16 [N,K] to be block-quantized."""
-    g = _gen(seed, device)
-    x = torch.randn(M, K, generator=g, device=device).to(torch.bfloat16)
-    w = (torch.randn(N, K, generator=g, device=device) * weight_std).to(torch.bfloat16)
+    x = torch.randn(M, K, generator=_gen(seed, device, 6), device=device).to(torch.bfloat16)
+    w = (torch.randn(N, K, generator=_gen(seed, device, 7), device=device) * weight_std).to(torch.bfloat16)
     return {"x": x.contiguous(), "w": w.contiguous()}
 
 
