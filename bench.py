@@ -211,6 +211,9 @@ def run_ours(args, rank, world):
     # per-kernel events recorded by the library around the two GEMMs
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for e4 in ev:           # materialize the CUDA events before the timed region
+        for e in e4:
+            e.record(stream)
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device()) as clk:

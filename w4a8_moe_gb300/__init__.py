@@ -202,6 +202,9 @@ def w4a8_set_profile_events(events) -> None:
     that moe_w4a8_forward records before/after its GEMMs on this host thread;
     None or [] switches recording off."""
     events = list(events or [])
+    for e in events:
+        if e.cuda_event == 0:  # torch creates the CUDA event on first record
+            e.record()
     arr = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
     _check(_load().w4a8_set_profile_events(arr, len(events)))
 

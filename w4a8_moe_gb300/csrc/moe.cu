@@ -55,21 +55,41 @@ struct MoeGemmParams {
     uint32_t* err;
 };
 
-template <int MODE, int BN, int KC, int PST, int AST>
+template <int MODE, int BN, int KC, int NST, bool ATMEM, int NCONV, int NACC>
 struct MoeTraits {
-    static constexpr int kAtoms = KC / 128;
-    static constexpr int kWBytes = 128 * KC / 2;
-    static constexpr int kBBytes = kAtoms * BN * 128;
-    static constexpr int kPBytes = kWBytes + kBBytes;
-    static constexpr int kABytes = kAtoms * 128 * 128;
-    static constexpr int kData = PST * kPBytes + AST * kABytes;
-    static constexpr int kBars = 2 * PST + 2 * AST + 4 + 1;  // + drain barrier
+    static constexpr int kAtoms = KC / 128;                      // 128-byte K atoms of A and B
+    static constexpr int kWBytes = 128 * KC / 2;                 // packed weights per stage
+    static constexpr int kWBoxBytes = KC == 128 ? 64 : 128;      // bytes per row per TMA box
+    static constexpr int kWBoxes = KC / 2 / kWBoxBytes;
+    static constexpr int kBBytes = kAtoms * BN * 128;            // activations per stage
+    static constexpr int kABytes = ATMEM ? 0 : kAtoms * 128 * 128;  // unpacked A in smem
+    static constexpr int kStage = kWBytes + kBBytes + kABytes;
+    static constexpr int kACols = KC / 4;                        // unpacked A in TMEM
+    static constexpr int kData = NST * kStage;
+    static constexpr int kBars = 3 * NST + 4 + 1;                // + drain barrier
     static constexpr int kCtrl = kBars * 8 + 16 + 4 * (256 + 260 + 260);
     static constexpr int kSmem = 1024 + kData + kCtrl;
-    static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
+    // two accumulator buffers (tile i / tile i+1), each NACC partial sums that
+    // take consecutive K-steps in turn
+    static constexpr int kDCols = 2 * NACC * BN;
+    static constexpr int kTmemNeed = kDCols + (ATMEM ? NST * kACols : 0);
+    static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
+                                   : kTmemNeed <= 256 ? 256 : 512;
+    static constexpr int kThreads = 32 * (8 + NCONV);
+    static constexpr int kEpi0 = 4 + NCONV;                      // first epilogue warp
+    static constexpr int kPar = NCONV / 4;                       // converter warps per quadrant
     static_assert(kWBytes % 1024 == 0 && kBBytes % 1024 == 0, "stage alignment");
     static_assert(kSmem <= 232448, "shared memory budget");
+    static_assert(kTmemNeed <= 512, "tensor memory budget");
     static_assert(BN % 16 == 0 && BN <= 256, "token tile");
+    static_assert(NCONV % 4 == 0 && NCONV >= 4, "converters cover the four TMEM lane quadrants");
+    static_assert(NACC == 1 || NACC == 2 || NACC == 4, "partial accumulators");
+    // Converter warp w takes the stages g with g % kPar == (w - 4) / 4 and waits
+    // on full[g % NST] by phase parity. A parity wait cannot tell phase r from
+    // r + 2, so every warp must see every round of each slot it serves: the
+    // ring depth must be a multiple of kPar (then slot s always maps to the
+    // same warp).
+    static_assert(NST % kPar == 0, "ring depth must be a multiple of the converter warps per quadrant");
 };
 
 struct TileInfo {
@@ -114,23 +134,30 @@ __device__ __forceinline__ float act_fn(float g, int act)
     return 0.5f * g * (1.0f + tanhf(c * (g + 0.044715f * g * g * g)));
 }
 
-template <int MODE, int BN, int KC, int PST, int AST>
-__global__ void __launch_bounds__(384, 1)
+// One ring of NST stages. Stage s holds the packed weights and activation tile
+// (shared memory, written by TMA) and the unpacked weights (TMEM or shared
+// memory, written by the converters). Per stage exactly three events happen:
+//   full[s]  TMA bytes landed                      -> converters
+//   afull[s] unpacked weights written (4 arrivals) -> MMA issuer
+//   done[s]  the stage's MMAs completed (commit)   -> producer
+// The converters need not wait for their A slot (the producer only refilled
+// stage s after done[s]), and the MMA need not wait for full[s] (the converters
+// observed it before arriving), so the single MMA thread spends one wait and
+// one commit per stage.
+template <int MODE, int BN, int KC, int NST, bool ATMEM, int NCONV, int NACC>
+__global__ void __launch_bounds__(32 * (8 + NCONV), 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b,
                     const MoeGemmParams p)
 {
-    using Tr = MoeTraits<MODE, BN, KC, PST, AST>;
+    using Tr = MoeTraits<MODE, BN, KC, NST, ATMEM, NCONV, NACC>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
-    uint8_t* pring = smem;
-    uint8_t* aring = smem + PST * Tr::kPBytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(aring + AST * Tr::kABytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Tr::kData);
     uint64_t* full = bars;
-    uint64_t* empty = full + PST;
-    uint64_t* afull = empty + PST;
-    uint64_t* aempty = afull + AST;
-    uint64_t* accfull = aempty + AST;
+    uint64_t* afull = full + NST;
+    uint64_t* done = afull + NST;
+    uint64_t* accfull = done + NST;
     uint64_t* accempty = accfull + 2;
     uint64_t* drain = accempty + 2;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain + 1);
@@ -143,13 +170,10 @@ __global__ void __launch_bounds__(384, 1)
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < PST; ++i) {
+        for (int i = 0; i < NST; ++i) {
             mbar_init(smem_u32(&full[i]), 1);
-            mbar_init(smem_u32(&empty[i]), 4 + 1);
-        }
-        for (int i = 0; i < AST; ++i) {
-            mbar_init(smem_u32(&afull[i]), 4);
-            mbar_init(smem_u32(&aempty[i]), 1);
+            mbar_init(smem_u32(&afull[i]), 4);   // one converter warp per lane quadrant
+            mbar_init(smem_u32(&done[i]), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&accfull[i]), 1);
@@ -182,6 +206,7 @@ __global__ void __launch_bounds__(384, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
+    const uint32_t tmem_a = tmem + Tr::kDCols;   // A slots (ATMEM)
     const int total = s_pre[p.E];
 
     auto fail = [&]() {
@@ -194,7 +219,7 @@ __global__ void __launch_bounds__(384, 1)
         if (lane == 0) {
             const uint64_t pol_w = policy_evict_first();
             const uint64_t pol_b = policy_evict_last();
-            int ps = 0;
+            int s = 0;
             uint32_t ph = 0;
             uint32_t issued = 0;       // bit s: stage s was filled at least once
             uint32_t last_par = 0;     // bit s: parity of the last fill of stage s
@@ -202,31 +227,37 @@ __global__ void __launch_bounds__(384, 1)
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 const TileInfo ti = decode_tile(t, s_cnt, s_off, s_pre, p.E, BN, p.ksplit);
                 for (int kb = 0; kb < p.kblocks; ++kb) {
-                    if (*s_abort || !mbar_wait(smem_u32(&empty[ps]), ph ^ 1u)) {
+                    if (*s_abort || !mbar_wait(smem_u32(&done[s]), ph ^ 1u)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t fb = smem_u32(&full[ps]);
-                    mbar_arrive_expect_tx(fb, Tr::kPBytes);
-                    uint8_t* st = pring + ps * Tr::kPBytes;
+                    const uint32_t fb = smem_u32(&full[s]);
+                    mbar_arrive_expect_tx(fb, Tr::kWBytes + Tr::kBBytes);
+                    uint8_t* st = smem + s * Tr::kStage;
                     const int kel = (ti.ks * p.kblocks + kb) * KC;  // first K element
-                    if (MODE == 0) {
-                        const int r0 = ti.e * p.rows_per_expert + ti.rt * 64;
-                        tma_load_2d_hint(smem_u32(st), &tm_w, kel / 2, r0, fb, pol_w);
-                        tma_load_2d_hint(smem_u32(st + Tr::kWBytes / 2), &tm_w, kel / 2, r0 + p.I, fb,
-                                         pol_w);
-                    } else {
-                        const int r0 = ti.e * p.rows_per_expert + ti.rt * 128;
-                        tma_load_2d_hint(smem_u32(st), &tm_w, kel / 2, r0, fb, pol_w);
+#pragma unroll
+                    for (int wa = 0; wa < Tr::kWBoxes; ++wa) {
+                        // one box = 128 rows x kWBoxBytes (gate_up: 64 gate + 64 up rows)
+                        uint8_t* wd = st + wa * 128 * Tr::kWBoxBytes;
+                        const int kx = kel / 2 + wa * Tr::kWBoxBytes;
+                        if (MODE == 0) {
+                            const int r0 = ti.e * p.rows_per_expert + ti.rt * 64;
+                            tma_load_2d_hint(smem_u32(wd), &tm_w, kx, r0, fb, pol_w);
+                            tma_load_2d_hint(smem_u32(wd + 64 * Tr::kWBoxBytes), &tm_w, kx, r0 + p.I, fb,
+                                             pol_w);
+                        } else {
+                            const int r0 = ti.e * p.rows_per_expert + ti.rt * 128;
+                            tma_load_2d_hint(smem_u32(wd), &tm_w, kx, r0, fb, pol_w);
+                        }
                     }
 #pragma unroll
                     for (int a = 0; a < Tr::kAtoms; ++a)
                         tma_load_2d_hint(smem_u32(st + Tr::kWBytes + a * BN * 128), &tm_b,
                                          kel + a * 128, ti.tok0, fb, pol_b);
-                    issued |= 1u << ps;
-                    last_par = (last_par & ~(1u << ps)) | (ph << ps);
-                    if (++ps == PST) {
-                        ps = 0;
+                    issued |= 1u << s;
+                    last_par = (last_par & ~(1u << s)) | (ph << s);
+                    if (++s == NST) {
+                        s = 0;
                         ph ^= 1u;
                     }
                 }
@@ -234,16 +265,16 @@ __global__ void __launch_bounds__(384, 1)
             if (!ok) {
                 fail();
                 // let every issued copy land before the CTA's shared memory goes away
-                for (int s = 0; s < PST; ++s)
-                    if ((issued >> s) & 1u)
-                        mbar_wait(smem_u32(&full[s]), (last_par >> s) & 1u);
+                for (int i = 0; i < NST; ++i)
+                    if ((issued >> i) & 1u)
+                        mbar_wait(smem_u32(&full[i]), (last_par >> i) & 1u);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            int ps = 0, as = 0;
-            uint32_t pph = 0, aph = 0;
+            int s = 0;
+            uint32_t ph = 0;
             int it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
@@ -257,32 +288,38 @@ __global__ void __launch_bounds__(384, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t dt = tmem + static_cast<uint32_t>(d * BN);
+                const uint32_t dt = tmem + static_cast<uint32_t>(d * NACC * BN);
                 for (int kb = 0; kb < p.kblocks; ++kb) {
-                    if (*s_abort || !mbar_wait(smem_u32(&full[ps]), pph) ||
-                        !mbar_wait(smem_u32(&afull[as]), aph)) {
+                    if (*s_abort || !mbar_wait(smem_u32(&afull[s]), ph)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t abase = smem_u32(aring + as * Tr::kABytes);
-                    const uint32_t bbase = smem_u32(pring + ps * Tr::kPBytes + Tr::kWBytes);
+                    const uint8_t* st = smem + s * Tr::kStage;
+                    const uint64_t bd0 = desc_kmajor_sw128(smem_u32(st + Tr::kWBytes));
+                    const uint64_t ad0 = ATMEM ? 0 : desc_kmajor_sw128(smem_u32(st + Tr::kWBytes + Tr::kBBytes));
 #pragma unroll
                     for (int kk = 0; kk < KC / 32; ++kk) {
                         const int atom = kk >> 2, sub = kk & 3;
-                        const uint64_t ad = desc_kmajor_sw128(abase + atom * (128 * 128) + sub * 32);
-                        const uint64_t bd = desc_kmajor_sw128(bbase + atom * (BN * 128) + sub * 32);
-                        umma_f8(dt, ad, bd, idesc, (kb | kk) ? 1u : 0u);
+                        // start-address field advances in 16-byte units
+                        const uint64_t bd = bd0 + static_cast<uint64_t>((atom * BN * 128 + sub * 32) >> 4);
+                        // K-step j goes to partial sum j % NACC; the first NACC
+                        // steps of the tile start their partial sums
+                        const int j = kb * (KC / 32) + kk;
+                        const uint32_t acc = (j >= NACC) ? 1u : 0u;
+                        const uint32_t dsub = dt + static_cast<uint32_t>((j % NACC) * BN);
+                        if (ATMEM) {
+                            umma_f8_ta(dsub, tmem_a + static_cast<uint32_t>(s * Tr::kACols + kk * 8), bd, idesc,
+                                       acc);
+                        } else {
+                            const uint64_t ad = ad0 + static_cast<uint64_t>((atom * 128 * 128 + sub * 32) >> 4);
+                            umma_f8(dsub, ad, bd, idesc, acc);
+                        }
                     }
-                    umma_commit(smem_u32(&empty[ps]));
-                    umma_commit(smem_u32(&aempty[as]));
-                    if (++ps == PST) {
-                        ps = 0;
-                        pph ^= 1u;
-                    }
-                    if (++as == AST) {
-                        as = 0;
-                        aph ^= 1u;
+                    umma_commit(smem_u32(&done[s]));
+                    if (++s == NST) {
+                        s = 0;
+                        ph ^= 1u;
                     }
                 }
                 if (!ok)
@@ -295,63 +332,81 @@ __global__ void __launch_bounds__(384, 1)
                 mbar_wait(smem_u32(drain), 0);
             }
         }
-    } else if (warp >= 4 && warp < 8) {
+    } else if (warp >= 4 && warp < Tr::kEpi0) {
         // ------------------------------------------------------------ converters
-        const int r = threadIdx.x - 128;  // A row == TMEM lane
+        // Warp w covers TMEM lane quadrant w % 4 (rows 32q..32q+31); with
+        // NCONV = 8 the two warps of a quadrant take alternate stages.
+        const int q = warp & 3;
+        const int par = (warp - 4) >> 2;
+        const int r = 32 * q + lane;  // A row == TMEM lane
         int src = r;
         if (MODE == 0) {
-            // lanes 0-15 of each 32-lane quadrant: gate rows; lanes 16-31: the
-            // matching up rows (so one warp holds both halves of a gated pair)
-            const int q = r >> 5, j = r & 31;
-            src = (j < 16) ? (16 * q + j) : (64 + 16 * q + (j - 16));
+            // lanes 0-15 of each quadrant: gate rows; lanes 16-31: the matching
+            // up rows (so one warp holds both halves of a gated pair)
+            src = (lane < 16) ? (16 * q + lane) : (64 + 16 * q + (lane - 16));
         }
-        int ps = 0, as = 0;
-        uint32_t pph = 0, aph = 0;
+        int s = 0;
+        uint32_t ph = 0;
+        uint32_t g = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            for (int kb = 0; kb < p.kblocks; ++kb) {
-                if (*s_abort || !mbar_wait(smem_u32(&full[ps]), pph) ||
-                    !mbar_wait(smem_u32(&aempty[as]), aph ^ 1u)) {
-                    ok = false;
-                    break;
-                }
-                const uint8_t* wrow = pring + ps * Tr::kPBytes + src * (KC / 2);
-                uint8_t* abase = aring + as * Tr::kABytes + r * 128;
+            for (int kb = 0; kb < p.kblocks; ++kb, ++g) {
+                if (static_cast<int>(g % Tr::kPar) == par) {
+                    if (*s_abort || !mbar_wait(smem_u32(&full[s]), ph)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint8_t* wst = smem + s * Tr::kStage;
 #pragma unroll
-                for (int c = 0; c < KC / 32; ++c) {
-                    // packed 16-byte chunk c of this row, after the TMA swizzle
-                    const int pc = (KC == 256) ? (c ^ (src & 7)) : (c ^ ((src >> 1) & 3));
-                    const uint4 w4 = *reinterpret_cast<const uint4*>(wrow + pc * 16);
-                    uint4 o0, o1;
-                    unpack8(w4.x, o0.x, o0.y);
-                    unpack8(w4.y, o0.z, o0.w);
-                    unpack8(w4.z, o1.x, o1.y);
-                    unpack8(w4.w, o1.z, o1.w);
-                    const int atom = (32 * c) >> 7;
-                    const int c16 = ((32 * c) & 127) >> 4;
-                    uint8_t* arow = abase + atom * (128 * 128);
-                    *reinterpret_cast<uint4*>(arow + ((c16 ^ (r & 7)) << 4)) = o0;
-                    *reinterpret_cast<uint4*>(arow + (((c16 + 1) ^ (r & 7)) << 4)) = o1;
+                    for (int half = 0; half < KC / 128; ++half) {
+                        uint32_t o[32];
+#pragma unroll
+                        for (int c4 = 0; c4 < 4; ++c4) {
+                            const int c = half * 4 + c4;  // packed 16-byte chunk (32 weights)
+                            // undo the TMA swizzle: 64-byte boxes (KC = 128) XOR chunk
+                            // bits with row bits 1-2, 128-byte boxes with row bits 0-2
+                            const uint8_t* wp =
+                                (KC == 128) ? wst + src * 64 + ((c ^ ((src >> 1) & 3)) << 4)
+                                            : wst + (c >> 3) * (128 * 128) + src * 128 + (((c & 7) ^ (src & 7)) << 4);
+                            const uint4 w4 = *reinterpret_cast<const uint4*>(wp);
+                            unpack8(w4.x, o[8 * c4 + 0], o[8 * c4 + 1]);
+                            unpack8(w4.y, o[8 * c4 + 2], o[8 * c4 + 3]);
+                            unpack8(w4.z, o[8 * c4 + 4], o[8 * c4 + 5]);
+                            unpack8(w4.w, o[8 * c4 + 6], o[8 * c4 + 7]);
+                        }
+                        if (ATMEM) {
+                            tmem_st32(tmem_a + (static_cast<uint32_t>(q * 32) << 16) +
+                                          static_cast<uint32_t>(s * Tr::kACols + half * 32),
+                                      o);
+                        } else {
+                            uint8_t* arow = smem + s * Tr::kStage + Tr::kWBytes + Tr::kBBytes +
+                                            half * (128 * 128) + r * 128;
+#pragma unroll
+                            for (int c16 = 0; c16 < 8; ++c16)
+                                *reinterpret_cast<uint4*>(arow + ((c16 ^ (r & 7)) << 4)) =
+                                    make_uint4(o[4 * c16], o[4 * c16 + 1], o[4 * c16 + 2], o[4 * c16 + 3]);
+                        }
+                    }
+                    if (ATMEM) {
+                        tmem_st_wait();
+                        tc_fence_before();
+                    } else {
+                        fence_proxy_async_smem();
+                    }
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(smem_u32(&afull[s]));
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(smem_u32(&afull[as]));
-                    mbar_arrive(smem_u32(&empty[ps]));
-                }
-                if (++ps == PST) {
-                    ps = 0;
-                    pph ^= 1u;
-                }
-                if (++as == AST) {
-                    as = 0;
-                    aph ^= 1u;
+                if (++s == NST) {
+                    s = 0;
+                    ph ^= 1u;
                 }
             }
         }
         if (!ok)
             fail();
-    } else if (warp >= 8) {
+    } else if (warp >= Tr::kEpi0) {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;
         const float a1 = __ldg(p.a1);
@@ -368,7 +423,23 @@ __global__ void __launch_bounds__(384, 1)
             }
             tc_fence_after();
             const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) +
-                                   static_cast<uint32_t>(d * BN);
+                                   static_cast<uint32_t>(d * NACC * BN);
+            // 32 accumulator columns starting at c, partial sums added in order
+            auto load_acc = [&](int c, uint32_t (&v)[32]) {
+                tmem_ld32(tbase + c, v);
+                if (NACC > 1) {
+                    uint32_t w[32];
+#pragma unroll
+                    for (int a = 1; a < NACC; ++a) {
+                        tmem_ld32(tbase + a * BN + c, w);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int x = 0; x < 32; ++x)
+                            v[x] = __float_as_uint(__uint_as_float(v[x]) + __uint_as_float(w[x]));
+                    }
+                }
+                tmem_ld_wait();
+            };
             const int nchunks = (ti.ntok + 31) >> 5;
             if (MODE == 0) {
                 const int half = lane >> 4;  // 0: gate lane, 1: up lane
@@ -377,8 +448,7 @@ __global__ void __launch_bounds__(384, 1)
                 const float su = a1 * __ldg(p.s_gu + static_cast<int64_t>(ti.e) * 2 * p.I + p.I + i);
                 for (int ch = 0; ch < nchunks; ++ch) {
                     uint32_t v[32];
-                    tmem_ld32(tbase + ch * 32, v);
-                    tmem_ld_wait();
+                    load_acc(ch * 32, v);
                     int s512[16];
 #pragma unroll
                     for (int cc = 0; cc < 16; ++cc) {
@@ -422,8 +492,7 @@ __global__ void __launch_bounds__(384, 1)
                 float* yb = p.ypart + (static_cast<int64_t>(ti.ks) * p.A + ti.tok0) * p.H + n;
                 for (int ch = 0; ch < nchunks; ++ch) {
                     uint32_t v[32];
-                    tmem_ld32(tbase + ch * 32, v);
-                    tmem_ld_wait();
+                    load_acc(ch * 32, v);
 #pragma unroll
                     for (int cc = 0; cc < 32; ++cc) {
                         const int col = ch * 32 + cc;
@@ -567,7 +636,12 @@ MoeConfig moe_pick_config(int T, int H, int I, int E, int k, int num_sms)
 {
     MoeConfig c;
     c.bn = pick_bn(T);
-    c.kc = (c.bn <= 64) ? 256 : 128;
+    // stage depth along K: longer stages amortize the per-stage barrier work
+    // of the single MMA thread; the decode tile takes 512 when H and I allow
+    if (c.bn == 32 && H % 512 == 0 && I % 512 == 0)
+        c.kc = 512;
+    else
+        c.kc = (c.bn <= 128) ? 256 : 128;
     // split the down projection's K so that its tiles fill the SMs evenly
     const int kblocks = I / c.kc;
     const int base_tiles = E * (H / 128);
@@ -589,28 +663,35 @@ MoeConfig moe_pick_config(int T, int H, int I, int E, int k, int num_sms)
     return c;
 }
 
-template <int MODE, int BN, int KC, int PST, int AST>
+template <int MODE, int BN, int KC, int NST, bool ATMEM, int NCONV, int NACC>
 static int launch_gemm(const CUtensorMap& tw, const CUtensorMap& tb, const MoeGemmParams& prm, int grid,
                        cudaStream_t s)
 {
-    using Tr = MoeTraits<MODE, BN, KC, PST, AST>;
-    auto kern = moe_gemm_kernel<MODE, BN, KC, PST, AST>;
+    using Tr = MoeTraits<MODE, BN, KC, NST, ATMEM, NCONV, NACC>;
+    auto kern = moe_gemm_kernel<MODE, BN, KC, NST, ATMEM, NCONV, NACC>;
     // attribute set on every launch: cheap, and correct for every device
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Tr::kSmem) != cudaSuccess)
         return kErrLaunch;
-    kern<<<grid, 384, Tr::kSmem, s>>>(tw, tb, prm);
+    kern<<<grid, Tr::kThreads, Tr::kSmem, s>>>(tw, tb, prm);
     return cudaGetLastError() == cudaSuccess ? kOK : kErrLaunch;
 }
 
+// Token tile -> pipeline shape. Up to 128 tokens the unpacked weights live in
+// tensor memory, which leaves shared memory to a deep TMA ring (192 KB); the
+// 256-token tile needs all of TMEM for its two accumulators and keeps A in
+// shared memory.
 template <int MODE>
 static int dispatch_gemm(const MoeConfig& cfg, const CUtensorMap& tw, const CUtensorMap& tb,
                          const MoeGemmParams& prm, int grid, cudaStream_t s)
 {
     switch (cfg.bn) {
-    case 32: return launch_gemm<MODE, 32, 256, 6, 2>(tw, tb, prm, grid, s);
-    case 64: return launch_gemm<MODE, 64, 256, 4, 2>(tw, tb, prm, grid, s);
-    case 128: return launch_gemm<MODE, 128, 128, 6, 2>(tw, tb, prm, grid, s);
-    default: return launch_gemm<MODE, 256, 128, 4, 2>(tw, tb, prm, grid, s);
+    case 32:
+        if (cfg.kc == 512)
+            return launch_gemm<MODE, 32, 512, 3, true, 4, 1>(tw, tb, prm, grid, s);
+        return launch_gemm<MODE, 32, 256, 7, true, 4, 1>(tw, tb, prm, grid, s);
+    case 64: return launch_gemm<MODE, 64, 256, 6, true, 8, 1>(tw, tb, prm, grid, s);
+    case 128: return launch_gemm<MODE, 128, 256, 4, true, 8, 1>(tw, tb, prm, grid, s);
+    default: return launch_gemm<MODE, 256, 128, 3, false, 4, 1>(tw, tb, prm, grid, s);
     }
 }
 
@@ -623,14 +704,16 @@ int launch_moe_forward(const MoeLaunch& L, const MoeConfig& cfg, int num_sms, cu
     if (cudaGetLastError() != cudaSuccess)
         return kErrLaunch;
 
-    const CUtensorMapSwizzle wsw = (KC == 256) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    // weight boxes: 64-byte rows (64-byte swizzle) for KC = 128, else 128-byte rows
+    const CUtensorMapSwizzle wsw = (KC == 128) ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+    const uint32_t wbox = (KC == 128) ? 64u : 128u;
     CUtensorMap tw_gu, tb_gu, tw_d, tb_d;
     if (!encode_map_2d(&tw_gu, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.w_gu, L.H / 2,
-                       static_cast<uint64_t>(L.E) * 2 * L.I, L.H / 2, KC / 2, 64, wsw) ||
+                       static_cast<uint64_t>(L.E) * 2 * L.I, L.H / 2, wbox, 64, wsw) ||
         !encode_map_2d(&tb_gu, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.xp, L.H, A, L.H, 128, BN,
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_map_2d(&tw_d, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.w_d, L.I / 2,
-                       static_cast<uint64_t>(L.E) * L.H, L.I / 2, KC / 2, 128, wsw) ||
+                       static_cast<uint64_t>(L.E) * L.H, L.I / 2, wbox, 128, wsw) ||
         !encode_map_2d(&tb_d, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.hq, L.I, A, L.I, 128, BN,
                        CU_TENSOR_MAP_SWIZZLE_128B))
         return kErrLaunch;
