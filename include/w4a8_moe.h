@@ -147,6 +147,43 @@ int moe_w4a8_forward(const uint8_t* x_e4m3, const float* a1_scale, int T, int H,
 size_t moe_w4a8_workspace_size(int T, int H, int I, int E, int k);
 
 /*
+ * moe_w4a8_forward_static -- moe_w4a8_forward for callers that cannot
+ * allocate device memory. The pages have no counterpart: this is a deployment
+ * variant of the same computation.
+ *
+ * Some callers have no allocator to give the library a workspace: a host
+ * application that owns the whole device-memory budget and hands plugins only
+ * their inputs and outputs, or a latency-critical loop that must never call
+ * cudaMalloc (which can synchronize the device or fail at an unpredictable
+ * moment). This entry point takes the same inputs and outputs as
+ * moe_w4a8_forward, minus ws/ws_bytes, and uses instead a scratch array of
+ * W4A8_STATIC_SCRATCH_BYTES that lives in the library's own device image: every
+ * GPU that loads the library reserves it until the process exits. It calls no
+ * allocating function.
+ *
+ *   - Problems whose moe_w4a8_workspace_size(T, H, I, E, k) exceeds
+ *     W4A8_STATIC_SCRATCH_BYTES return W4A8_ERR_WORKSPACE (use
+ *     moe_w4a8_forward with a caller workspace for those); that covers
+ *     decode-sized layers (e.g. 32 tokens of a Grok-1-shaped layer).
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture on the device.
+ *   - All calls on a device share the one array and it keeps the last call's
+ *     contents; the state each call needs cleared is cleared by the call's
+ *     first kernel. Calls whose kernels overlap on the GPU (concurrent streams,
+ *     or host threads using the same device) race on the array: serialize
+ *     them, e.g. on one stream.
+ *   - A bounded device wait that runs out is not reported by this variant.
+ */
+#define W4A8_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
+int moe_w4a8_forward_static(const uint8_t* x_e4m3, const float* a1_scale, int T, int H, int I,
+                            int E, int k, const int32_t* w_gu, const float* s_gu,
+                            const int32_t* w_d, const float* s_d, const float* a2_scale, int act,
+                            const int32_t* topk_ids, const float* topk_w, const int32_t* counts,
+                            const int32_t* offsets, const int32_t* sorted_ids,
+                            const int32_t* inv_perm, uint16_t* out_bf16, void* stream);
+
+/*
  * fp8_block_linear -- block-FP8 dense projection y = x W^T (PR #392
  * description: FP8_PB_WO weights consumed with their weight_scale_inv, one
  * fp32 scale per 128-row x 128-col block).
