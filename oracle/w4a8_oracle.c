@@ -24,7 +24,7 @@
  *   OCP 8-bit Floating Point Specification (OFP8), format E4M3: the fp8
  *   format the pages' "fp8" denotes on hardware with /448 saturation.
  *
- * Readings where the pages are silent are listed in the design doc and restated
+ * Readings taken where the pages are silent are stated
  * next to each function below.
  *
  * Precision: floating point that only feeds a sum is carried in double;
