@@ -55,7 +55,7 @@ struct MoeGemmParams {
     uint32_t* err;
 };
 
-template <int MODE, int BN, int KC, int NST, bool ATMEM, int NCONV, int NACC>
+template <int MODE, int BN, int KC, int NW, int NX, bool ATMEM, int NCONV>
 struct MoeTraits {
     static constexpr int kAtoms = KC / 128;                      // 128-byte K atoms of A and B
     static constexpr int kWBytes = 128 * KC / 2;                 // packed weights per stage
@@ -63,33 +63,30 @@ struct MoeTraits {
     static constexpr int kWBoxes = KC / 2 / kWBoxBytes;
     static constexpr int kBBytes = kAtoms * BN * 128;            // activations per stage
     static constexpr int kABytes = ATMEM ? 0 : kAtoms * 128 * 128;  // unpacked A in smem
-    static constexpr int kStage = kWBytes + kBBytes + kABytes;
+    static constexpr int kXBytes = kBBytes + kABytes;
     static constexpr int kACols = KC / 4;                        // unpacked A in TMEM
-    static constexpr int kData = NST * kStage;
-    static constexpr int kBars = 3 * NST + 4 + 1;                // + drain barrier
+    static constexpr int kData = NW * kWBytes + NX * kXBytes;
+    static constexpr int kBars = 2 * NW + 3 * NX + 4 + 1;        // + drain barrier
     static constexpr int kCtrl = kBars * 8 + 16 + 4 * (256 + 260 + 260);
     static constexpr int kSmem = 1024 + kData + kCtrl;
-    // two accumulator buffers (tile i / tile i+1), each NACC partial sums that
-    // take consecutive K-steps in turn
-    static constexpr int kDCols = 2 * NACC * BN;
-    static constexpr int kTmemNeed = kDCols + (ATMEM ? NST * kACols : 0);
+    static constexpr int kDCols = 2 * BN;                        // two accumulators
+    static constexpr int kTmemNeed = kDCols + (ATMEM ? NX * kACols : 0);
     static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
                                    : kTmemNeed <= 256 ? 256 : 512;
     static constexpr int kThreads = 32 * (8 + NCONV);
     static constexpr int kEpi0 = 4 + NCONV;                      // first epilogue warp
     static constexpr int kPar = NCONV / 4;                       // converter warps per quadrant
-    static_assert(kWBytes % 1024 == 0 && kBBytes % 1024 == 0, "stage alignment");
+    static_assert(kWBytes % 1024 == 0 && kXBytes % 1024 == 0, "stage alignment");
     static_assert(kSmem <= 232448, "shared memory budget");
     static_assert(kTmemNeed <= 512, "tensor memory budget");
     static_assert(BN % 16 == 0 && BN <= 256, "token tile");
     static_assert(NCONV % 4 == 0 && NCONV >= 4, "converters cover the four TMEM lane quadrants");
-    static_assert(NACC == 1 || NACC == 2 || NACC == 4, "partial accumulators");
     // Converter warp w takes the stages g with g % kPar == (w - 4) / 4 and waits
-    // on full[g % NST] by phase parity. A parity wait cannot tell phase r from
-    // r + 2, so every warp must see every round of each slot it serves: the
-    // ring depth must be a multiple of kPar (then slot s always maps to the
-    // same warp).
-    static_assert(NST % kPar == 0, "ring depth must be a multiple of the converter warps per quadrant");
+    // on the rings' barriers by phase parity. A parity wait cannot tell phase r
+    // from r + 2, so every warp must see every round of each slot it serves:
+    // both ring depths must be multiples of kPar (then a slot always maps to
+    // the same warp).
+    static_assert(NW % kPar == 0 && NX % kPar == 0, "ring depths must be multiples of the converter warps per quadrant");
 };
 
 struct TileInfo {
@@ -117,13 +114,22 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const int* s_cnt, const i
     return ti;
 }
 
-// Nibbles -> E4M3 operand bytes worth (q + 8) * 2^-9, in K order.
+// Nibbles -> E4M3 operand bytes worth (q + 8) * 2^-9. The two output words
+// hold the weights of one packed word in the order [0,2,4,6 | 1,3,5,7]: the
+// K order inside every group of 8 is permuted, and the activation operands
+// (gathered x, and hq written by the gate_up epilogue) are stored with the same
+// permutation, so the dot products are unchanged and the unpack costs one
+// shift and two AND/XOR per 8 weights.
 __device__ __forceinline__ void unpack8(uint32_t w, uint32_t& lo4, uint32_t& hi4)
 {
-    const uint32_t ev = (w & 0x0F0F0F0Fu) ^ 0x08080808u;         // codes 0,2,4,6
-    const uint32_t od = ((w >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;  // codes 1,3,5,7
-    lo4 = prmt(ev, od, 0x5140u);                                 // 0,1,2,3
-    hi4 = prmt(ev, od, 0x7362u);                                 // 4,5,6,7
+    lo4 = (w & 0x0F0F0F0Fu) ^ 0x08080808u;          // codes 0,2,4,6
+    hi4 = ((w >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;   // codes 1,3,5,7
+}
+
+// Position of element i inside its group of 8 in the permuted K order.
+__device__ __forceinline__ int kperm(int i)
+{
+    return (i & ~7) | ((i & 7) >> 1) | ((i & 1) << 2);
 }
 
 __device__ __forceinline__ float act_fn(float g, int act)
@@ -134,30 +140,36 @@ __device__ __forceinline__ float act_fn(float g, int act)
     return 0.5f * g * (1.0f + tanhf(c * (g + 0.044715f * g * g * g)));
 }
 
-// One ring of NST stages. Stage s holds the packed weights and activation tile
-// (shared memory, written by TMA) and the unpacked weights (TMEM or shared
-// memory, written by the converters). Per stage exactly three events happen:
-//   full[s]  TMA bytes landed                      -> converters
-//   afull[s] unpacked weights written (4 arrivals) -> MMA issuer
-//   done[s]  the stage's MMAs completed (commit)   -> producer
-// The converters need not wait for their A slot (the producer only refilled
-// stage s after done[s]), and the MMA need not wait for full[s] (the converters
-// observed it before arriving), so the single MMA thread spends one wait and
-// one commit per stage.
-template <int MODE, int BN, int KC, int NST, bool ATMEM, int NCONV, int NACC>
+// Two rings, both indexed by the global stage number g of this CTA.
+//   W ring (NW slots, shared memory): packed weights. TMA -> wfull[w];
+//     converters read the slot and free it at once (wfree[w]), so a weight slot
+//     is held only for the HBM latency plus the conversion.
+//   X ring (NX slots): the activation tile (shared memory, TMA -> bfull[x])
+//     and the unpacked weights (TMEM, or shared memory, converters ->
+//     afull[x]); the MMA's commit frees both (xfree[x]).
+// Warp 0 issues weight copies as far ahead as the W ring allows; warp 2 issues
+// activation copies, gated by xfree. A converter waits on bfull[x] as well,
+// which both guarantees its A slot is free (bfull round r follows xfree round
+// r-1) and lets the MMA wait on afull alone: one wait and one commit per stage
+// in the single MMA thread.
+template <int MODE, int BN, int KC, int NW, int NX, bool ATMEM, int NCONV>
 __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b,
                     const MoeGemmParams p)
 {
-    using Tr = MoeTraits<MODE, BN, KC, NST, ATMEM, NCONV, NACC>;
+    using Tr = MoeTraits<MODE, BN, KC, NW, NX, ATMEM, NCONV>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
+    uint8_t* wring = smem;
+    uint8_t* xring = smem + NW * Tr::kWBytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Tr::kData);
-    uint64_t* full = bars;
-    uint64_t* afull = full + NST;
-    uint64_t* done = afull + NST;
-    uint64_t* accfull = done + NST;
+    uint64_t* wfull = bars;
+    uint64_t* wfree = wfull + NW;
+    uint64_t* bfull = wfree + NW;
+    uint64_t* afull = bfull + NX;
+    uint64_t* xfree = afull + NX;
+    uint64_t* accfull = xfree + NX;
     uint64_t* accempty = accfull + 2;
     uint64_t* drain = accempty + 2;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain + 1);
@@ -170,10 +182,14 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < NST; ++i) {
-            mbar_init(smem_u32(&full[i]), 1);
-            mbar_init(smem_u32(&afull[i]), 4);   // one converter warp per lane quadrant
-            mbar_init(smem_u32(&done[i]), 1);
+        for (int i = 0; i < NW; ++i) {
+            mbar_init(smem_u32(&wfull[i]), 1);
+            mbar_init(smem_u32(&wfree[i]), 4);   // one converter warp per lane quadrant
+        }
+        for (int i = 0; i < NX; ++i) {
+            mbar_init(smem_u32(&bfull[i]), 1);
+            mbar_init(smem_u32(&afull[i]), 4);
+            mbar_init(smem_u32(&xfree[i]), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&accfull[i]), 1);
@@ -214,49 +230,56 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
         set_error(p.err, kErrBitTimeout);
     };
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
+    if (warp == 0 || warp == 2) {
+        // ------------------------------------------------------------ producers
+        // warp 0: packed weights into the W ring; warp 2: activations into the X ring
         if (lane == 0) {
-            const uint64_t pol_w = policy_evict_first();
-            const uint64_t pol_b = policy_evict_last();
+            const bool wprod = (warp == 0);
+            const int nslot = wprod ? NW : NX;
+            uint64_t* fullb = wprod ? wfull : bfull;
+            uint64_t* freeb = wprod ? wfree : xfree;
+            const uint64_t pol = wprod ? policy_evict_first() : policy_evict_last();
             int s = 0;
             uint32_t ph = 0;
-            uint32_t issued = 0;       // bit s: stage s was filled at least once
-            uint32_t last_par = 0;     // bit s: parity of the last fill of stage s
+            uint32_t issued = 0;       // bit s: slot s was filled at least once
+            uint32_t last_par = 0;     // bit s: parity of the last fill of slot s
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 const TileInfo ti = decode_tile(t, s_cnt, s_off, s_pre, p.E, BN, p.ksplit);
                 for (int kb = 0; kb < p.kblocks; ++kb) {
-                    if (*s_abort || !mbar_wait(smem_u32(&done[s]), ph ^ 1u)) {
+                    if (!mbar_wait_or_abort(smem_u32(&freeb[s]), ph ^ 1u, s_abort)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t fb = smem_u32(&full[s]);
-                    mbar_arrive_expect_tx(fb, Tr::kWBytes + Tr::kBBytes);
-                    uint8_t* st = smem + s * Tr::kStage;
+                    const uint32_t fb = smem_u32(&fullb[s]);
                     const int kel = (ti.ks * p.kblocks + kb) * KC;  // first K element
+                    if (wprod) {
+                        mbar_arrive_expect_tx(fb, Tr::kWBytes);
+                        uint8_t* st = wring + s * Tr::kWBytes;
 #pragma unroll
-                    for (int wa = 0; wa < Tr::kWBoxes; ++wa) {
-                        // one box = 128 rows x kWBoxBytes (gate_up: 64 gate + 64 up rows)
-                        uint8_t* wd = st + wa * 128 * Tr::kWBoxBytes;
-                        const int kx = kel / 2 + wa * Tr::kWBoxBytes;
-                        if (MODE == 0) {
-                            const int r0 = ti.e * p.rows_per_expert + ti.rt * 64;
-                            tma_load_2d_hint(smem_u32(wd), &tm_w, kx, r0, fb, pol_w);
-                            tma_load_2d_hint(smem_u32(wd + 64 * Tr::kWBoxBytes), &tm_w, kx, r0 + p.I, fb,
-                                             pol_w);
-                        } else {
-                            const int r0 = ti.e * p.rows_per_expert + ti.rt * 128;
-                            tma_load_2d_hint(smem_u32(wd), &tm_w, kx, r0, fb, pol_w);
+                        for (int wa = 0; wa < Tr::kWBoxes; ++wa) {
+                            // one box = 128 rows x kWBoxBytes (gate_up: 64 gate + 64 up rows)
+                            uint8_t* wd = st + wa * 128 * Tr::kWBoxBytes;
+                            const int kx = kel / 2 + wa * Tr::kWBoxBytes;
+                            if (MODE == 0) {
+                                const int r0 = ti.e * p.rows_per_expert + ti.rt * 64;
+                                tma_load_2d_hint(smem_u32(wd), &tm_w, kx, r0, fb, pol);
+                                tma_load_2d_hint(smem_u32(wd + 64 * Tr::kWBoxBytes), &tm_w, kx, r0 + p.I, fb, pol);
+                            } else {
+                                const int r0 = ti.e * p.rows_per_expert + ti.rt * 128;
+                                tma_load_2d_hint(smem_u32(wd), &tm_w, kx, r0, fb, pol);
+                            }
                         }
-                    }
+                    } else {
+                        mbar_arrive_expect_tx(fb, Tr::kBBytes);
+                        uint8_t* st = xring + s * Tr::kXBytes;
 #pragma unroll
-                    for (int a = 0; a < Tr::kAtoms; ++a)
-                        tma_load_2d_hint(smem_u32(st + Tr::kWBytes + a * BN * 128), &tm_b,
-                                         kel + a * 128, ti.tok0, fb, pol_b);
+                        for (int a = 0; a < Tr::kAtoms; ++a)
+                            tma_load_2d_hint(smem_u32(st + a * BN * 128), &tm_b, kel + a * 128, ti.tok0, fb, pol);
+                    }
                     issued |= 1u << s;
                     last_par = (last_par & ~(1u << s)) | (ph << s);
-                    if (++s == NST) {
+                    if (++s == nslot) {
                         s = 0;
                         ph ^= 1u;
                     }
@@ -265,15 +288,15 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
             if (!ok) {
                 fail();
                 // let every issued copy land before the CTA's shared memory goes away
-                for (int i = 0; i < NST; ++i)
+                for (int i = 0; i < nslot; ++i)
                     if ((issued >> i) & 1u)
-                        mbar_wait(smem_u32(&full[i]), (last_par >> i) & 1u);
+                        mbar_wait(smem_u32(&fullb[i]), (last_par >> i) & 1u);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            int s = 0;
+            int x = 0;
             uint32_t ph = 0;
             int it = 0;
             bool ok = true;
@@ -283,42 +306,37 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                 const uint32_t idesc = idesc_e4m3_f32(128, nmma);
                 const int d = it & 1;
                 const uint32_t use = static_cast<uint32_t>(it >> 1);
-                if (*s_abort || !mbar_wait(smem_u32(&accempty[d]), (use & 1u) ^ 1u)) {
+                if (!mbar_wait_or_abort(smem_u32(&accempty[d]), (use & 1u) ^ 1u, s_abort)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t dt = tmem + static_cast<uint32_t>(d * NACC * BN);
+                const uint32_t dt = tmem + static_cast<uint32_t>(d * BN);
                 for (int kb = 0; kb < p.kblocks; ++kb) {
-                    if (*s_abort || !mbar_wait(smem_u32(&afull[s]), ph)) {
+                    if (!mbar_wait_or_abort(smem_u32(&afull[x]), ph, s_abort)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint8_t* st = smem + s * Tr::kStage;
-                    const uint64_t bd0 = desc_kmajor_sw128(smem_u32(st + Tr::kWBytes));
-                    const uint64_t ad0 = ATMEM ? 0 : desc_kmajor_sw128(smem_u32(st + Tr::kWBytes + Tr::kBBytes));
+                    const uint8_t* st = xring + x * Tr::kXBytes;
+                    const uint64_t bd0 = desc_kmajor_sw128(smem_u32(st));
+                    const uint64_t ad0 = ATMEM ? 0 : desc_kmajor_sw128(smem_u32(st + Tr::kBBytes));
 #pragma unroll
                     for (int kk = 0; kk < KC / 32; ++kk) {
                         const int atom = kk >> 2, sub = kk & 3;
                         // start-address field advances in 16-byte units
                         const uint64_t bd = bd0 + static_cast<uint64_t>((atom * BN * 128 + sub * 32) >> 4);
-                        // K-step j goes to partial sum j % NACC; the first NACC
-                        // steps of the tile start their partial sums
-                        const int j = kb * (KC / 32) + kk;
-                        const uint32_t acc = (j >= NACC) ? 1u : 0u;
-                        const uint32_t dsub = dt + static_cast<uint32_t>((j % NACC) * BN);
+                        const uint32_t acc = (kb | kk) ? 1u : 0u;
                         if (ATMEM) {
-                            umma_f8_ta(dsub, tmem_a + static_cast<uint32_t>(s * Tr::kACols + kk * 8), bd, idesc,
-                                       acc);
+                            umma_f8_ta(dt, tmem_a + static_cast<uint32_t>(x * Tr::kACols + kk * 8), bd, idesc, acc);
                         } else {
                             const uint64_t ad = ad0 + static_cast<uint64_t>((atom * 128 * 128 + sub * 32) >> 4);
-                            umma_f8(dsub, ad, bd, idesc, acc);
+                            umma_f8(dt, ad, bd, idesc, acc);
                         }
                     }
-                    umma_commit(smem_u32(&done[s]));
-                    if (++s == NST) {
-                        s = 0;
+                    umma_commit(smem_u32(&xfree[x]));
+                    if (++x == NX) {
+                        x = 0;
                         ph ^= 1u;
                     }
                 }
@@ -345,19 +363,20 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
             // up rows (so one warp holds both halves of a gated pair)
             src = (lane < 16) ? (16 * q + lane) : (64 + 16 * q + (lane - 16));
         }
-        int s = 0;
-        uint32_t ph = 0;
+        int w = 0, x = 0;
+        uint32_t wph = 0, xph = 0;
         uint32_t g = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
             for (int kb = 0; kb < p.kblocks; ++kb, ++g) {
                 if (static_cast<int>(g % Tr::kPar) == par) {
-                    if (*s_abort || !mbar_wait(smem_u32(&full[s]), ph)) {
+                    if (!mbar_wait_or_abort(smem_u32(&wfull[w]), wph, s_abort) ||
+                        !mbar_wait_or_abort(smem_u32(&bfull[x]), xph, s_abort)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint8_t* wst = smem + s * Tr::kStage;
+                    const uint8_t* wst = wring + w * Tr::kWBytes;
 #pragma unroll
                     for (int half = 0; half < KC / 128; ++half) {
                         uint32_t o[32];
@@ -377,17 +396,20 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                         }
                         if (ATMEM) {
                             tmem_st32(tmem_a + (static_cast<uint32_t>(q * 32) << 16) +
-                                          static_cast<uint32_t>(s * Tr::kACols + half * 32),
+                                          static_cast<uint32_t>(x * Tr::kACols + half * 32),
                                       o);
                         } else {
-                            uint8_t* arow = smem + s * Tr::kStage + Tr::kWBytes + Tr::kBBytes +
-                                            half * (128 * 128) + r * 128;
+                            uint8_t* arow = xring + x * Tr::kXBytes + Tr::kBBytes + half * (128 * 128) + r * 128;
 #pragma unroll
                             for (int c16 = 0; c16 < 8; ++c16)
                                 *reinterpret_cast<uint4*>(arow + ((c16 ^ (r & 7)) << 4)) =
                                     make_uint4(o[4 * c16], o[4 * c16 + 1], o[4 * c16 + 2], o[4 * c16 + 3]);
                         }
                     }
+                    // the packed slot has been read: hand it back to the producer now
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(smem_u32(&wfree[w]));
                     if (ATMEM) {
                         tmem_st_wait();
                         tc_fence_before();
@@ -396,11 +418,15 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                     }
                     __syncwarp();
                     if (lane == 0)
-                        mbar_arrive(smem_u32(&afull[s]));
+                        mbar_arrive(smem_u32(&afull[x]));
                 }
-                if (++s == NST) {
-                    s = 0;
-                    ph ^= 1u;
+                if (++w == NW) {
+                    w = 0;
+                    wph ^= 1u;
+                }
+                if (++x == NX) {
+                    x = 0;
+                    xph ^= 1u;
                 }
             }
         }
@@ -417,27 +443,15 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
             const TileInfo ti = decode_tile(t, s_cnt, s_off, s_pre, p.E, BN, p.ksplit);
             const int d = it & 1;
             const uint32_t use = static_cast<uint32_t>(it >> 1);
-            if (*s_abort || !mbar_wait(smem_u32(&accfull[d]), use & 1u)) {
+            if (!mbar_wait_or_abort(smem_u32(&accfull[d]), use & 1u, s_abort)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) +
-                                   static_cast<uint32_t>(d * NACC * BN);
-            // 32 accumulator columns starting at c, partial sums added in order
+                                   static_cast<uint32_t>(d * BN);
             auto load_acc = [&](int c, uint32_t (&v)[32]) {
                 tmem_ld32(tbase + c, v);
-                if (NACC > 1) {
-                    uint32_t w[32];
-#pragma unroll
-                    for (int a = 1; a < NACC; ++a) {
-                        tmem_ld32(tbase + a * BN + c, w);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int x = 0; x < 32; ++x)
-                            v[x] = __float_as_uint(__uint_as_float(v[x]) + __uint_as_float(w[x]));
-                    }
-                }
                 tmem_ld_wait();
             };
             const int nchunks = (ti.ntok + 31) >> 5;
@@ -466,7 +480,7 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                             const float U = fmaf(512.0f, pu, -shift);
                             const float h = act_fn(sg * G, p.act) * (su * U);
                             const uint32_t code = cvt_e4m3(__fdiv_rn(h, a2));
-                            p.hq[static_cast<int64_t>(pos) * p.I + i] = static_cast<uint8_t>(code);
+                            p.hq[static_cast<int64_t>(pos) * p.I + kperm(i)] = static_cast<uint8_t>(code);
                             s512[cc] = e4m3_times512(code);
                         }
                     }
@@ -520,7 +534,8 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
 }
 
 // ---------------------------------------------------------------------------
-// Gather: xp[pos] = x[sorted[pos] / k]; s0x[pos] = sum_h 512*dec(x) (exact);
+// Gather: xp[pos] = x[sorted[pos] / k] (bytes in the permuted K order of
+// unpack8); s0x[pos] = sum_h 512*dec(x) (exact);
 // s0h[pos] = 0 (the gate_up epilogue accumulates into it).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) moe_gather_kernel(const uint8_t* __restrict__ xq, int H, int k,
@@ -539,7 +554,9 @@ __global__ void __launch_bounds__(256) moe_gather_kernel(const uint8_t* __restri
     long long sum = 0;
     for (int c = lane; c < H / 16; c += 32) {
         const uint4 v = __ldg(src + c);
-        dst[c] = v;
+        // permuted K order inside each group of 8 (see unpack8)
+        dst[c] = make_uint4(prmt(v.x, v.y, 0x6420u), prmt(v.x, v.y, 0x7531u), prmt(v.z, v.w, 0x6420u),
+                            prmt(v.z, v.w, 0x7531u));
         const uint32_t u[4] = {v.x, v.y, v.z, v.w};
         int s = 0;
 #pragma unroll
@@ -663,12 +680,12 @@ MoeConfig moe_pick_config(int T, int H, int I, int E, int k, int num_sms)
     return c;
 }
 
-template <int MODE, int BN, int KC, int NST, bool ATMEM, int NCONV, int NACC>
+template <int MODE, int BN, int KC, int NW, int NX, bool ATMEM, int NCONV>
 static int launch_gemm(const CUtensorMap& tw, const CUtensorMap& tb, const MoeGemmParams& prm, int grid,
                        cudaStream_t s)
 {
-    using Tr = MoeTraits<MODE, BN, KC, NST, ATMEM, NCONV, NACC>;
-    auto kern = moe_gemm_kernel<MODE, BN, KC, NST, ATMEM, NCONV, NACC>;
+    using Tr = MoeTraits<MODE, BN, KC, NW, NX, ATMEM, NCONV>;
+    auto kern = moe_gemm_kernel<MODE, BN, KC, NW, NX, ATMEM, NCONV>;
     // attribute set on every launch: cheap, and correct for every device
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Tr::kSmem) != cudaSuccess)
         return kErrLaunch;
@@ -687,11 +704,11 @@ static int dispatch_gemm(const MoeConfig& cfg, const CUtensorMap& tw, const CUte
     switch (cfg.bn) {
     case 32:
         if (cfg.kc == 512)
-            return launch_gemm<MODE, 32, 512, 3, true, 4, 1>(tw, tb, prm, grid, s);
-        return launch_gemm<MODE, 32, 256, 7, true, 4, 1>(tw, tb, prm, grid, s);
-    case 64: return launch_gemm<MODE, 64, 256, 6, true, 8, 1>(tw, tb, prm, grid, s);
-    case 128: return launch_gemm<MODE, 128, 256, 4, true, 8, 1>(tw, tb, prm, grid, s);
-    default: return launch_gemm<MODE, 256, 128, 3, false, 4, 1>(tw, tb, prm, grid, s);
+            return launch_gemm<MODE, 32, 512, 5, 3, true, 4>(tw, tb, prm, grid, s);
+        return launch_gemm<MODE, 32, 256, 10, 6, true, 4>(tw, tb, prm, grid, s);
+    case 64: return launch_gemm<MODE, 64, 256, 8, 4, true, 8>(tw, tb, prm, grid, s);
+    case 128: return launch_gemm<MODE, 128, 256, 4, 4, true, 8>(tw, tb, prm, grid, s);
+    default: return launch_gemm<MODE, 256, 128, 8, 3, false, 4>(tw, tb, prm, grid, s);
     }
 }
 

@@ -65,6 +65,25 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
     return false;
 }
 
+// Same, but also gives up as soon as another role of the CTA has set *abort
+// (checked only while spinning, so a phase that is already complete costs one
+// try_wait).
+__device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity, const volatile int* abort)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const long long t0 = clock64();
+    for (uint32_t it = 0; it < kWaitMaxPolls; ++it) {
+        if (*abort)
+            return false;
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if (clock64() - t0 > kWaitBudgetCycles)
+            break;
+    }
+    return false;
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
