@@ -229,6 +229,7 @@ def run_ours(args, rank, world):
     ms_total = max_over_ranks(ms_total, world)
     ms_gu = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     ms_dn = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    ms_fin = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
     assert lib.w4a8_device_error(ws) == 0, "device error word set"
 
     # end to end through the public API with host buffers: H2D of the step's
@@ -266,7 +267,9 @@ def run_ours(args, rank, world):
                 "h2d_bytes_per_step": hx.numel() * 2 + hl.numel() * 4,
                 "d2h_bytes_per_step": hout.numel() * 2},
         "clocks": clk.summary(),
-        "kernels": {"gate_up_ms": ms_gu, "down_ms": ms_dn, "gate_up_bytes": gu_bytes,
+        "kernels": {"gate_up_ms": ms_gu, "down_ms": ms_dn, "finalize_ms": ms_fin,
+                    "route_gather_gaps_ms": ms_total / args.steps - ms_gu - ms_dn - ms_fin,
+                    "gate_up_bytes": gu_bytes,
                     "down_bytes": d_bytes, "act_bytes": act_bytes,
                     "active_experts": sum(1 for c in counts if c > 0)},
         "shape": shape,
@@ -361,7 +364,10 @@ def main():
             "traffic": None,
             "per_launch_ms": kk["gate_up_ms"], "algorithmic_bytes": kk["gate_up_bytes"],
             "down": {"per_launch_ms": kk["down_ms"], "algorithmic_bytes": kk["down_bytes"],
-                     "achieved": kk["down_bytes"] / (kk["down_ms"] * 1e-3) / 1e9}}
+                     "achieved": kk["down_bytes"] / (kk["down_ms"] * 1e-3) / 1e9},
+            "step_breakdown_ms": {"gate_up": kk["gate_up_ms"], "down": kk["down_ms"],
+                                  "finalize": kk["finalize_ms"],
+                                  "route_gather_and_gaps": kk["route_gather_gaps_ms"]}}
     layer_bytes = kk["gate_up_bytes"] + kk["down_bytes"] + kk["act_bytes"]
     line = {"metric": METRIC, "value": res["value"], "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],

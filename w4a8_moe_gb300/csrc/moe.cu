@@ -55,7 +55,7 @@ struct MoeGemmParams {
     uint32_t* err;
 };
 
-template <int MODE, int BN, int KC, int NW, int NX, bool ATMEM, int NCONV>
+template <int MODE, int BN, int KC, int NW, int NX, bool ATMEM, int NCONV, int NISS>
 struct MoeTraits {
     static constexpr int kAtoms = KC / 128;                      // 128-byte K atoms of A and B
     static constexpr int kWBytes = 128 * KC / 2;                 // packed weights per stage
@@ -66,10 +66,12 @@ struct MoeTraits {
     static constexpr int kXBytes = kBBytes + kABytes;
     static constexpr int kACols = KC / 4;                        // unpacked A in TMEM
     static constexpr int kData = NW * kWBytes + NX * kXBytes;
-    static constexpr int kBars = 2 * NW + 3 * NX + 4 + 1;        // + drain barrier
+    static constexpr int kBars = 2 * NW + 3 * NX + 4 + 2;        // + drain barriers
     static constexpr int kCtrl = kBars * 8 + 16 + 4 * (256 + 260 + 260);
     static constexpr int kSmem = 1024 + kData + kCtrl;
-    static constexpr int kDCols = 2 * BN;                        // two accumulators
+    // two accumulator buffers (tile i / tile i+1), each with one partial sum
+    // per MMA-issuing thread
+    static constexpr int kDCols = 2 * NISS * BN;
     static constexpr int kTmemNeed = kDCols + (ATMEM ? NX * kACols : 0);
     static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
                                    : kTmemNeed <= 256 ? 256 : 512;
@@ -87,6 +89,9 @@ struct MoeTraits {
     // both ring depths must be multiples of kPar (then a slot always maps to
     // the same warp).
     static_assert(NW % kPar == 0 && NX % kPar == 0, "ring depths must be multiples of the converter warps per quadrant");
+    // MMA issuer i takes the stages g with g % NISS == i and waits on afull by
+    // parity as well, so the X ring depth must be a multiple of NISS.
+    static_assert((NISS == 1 || NISS == 2) && NX % NISS == 0, "MMA issuers");
 };
 
 struct TileInfo {
@@ -152,12 +157,12 @@ __device__ __forceinline__ float act_fn(float g, int act)
 // which both guarantees its A slot is free (bfull round r follows xfree round
 // r-1) and lets the MMA wait on afull alone: one wait and one commit per stage
 // in the single MMA thread.
-template <int MODE, int BN, int KC, int NW, int NX, bool ATMEM, int NCONV>
+template <int MODE, int BN, int KC, int NW, int NX, bool ATMEM, int NCONV, int NISS>
 __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b,
                     const MoeGemmParams p)
 {
-    using Tr = MoeTraits<MODE, BN, KC, NW, NX, ATMEM, NCONV>;
+    using Tr = MoeTraits<MODE, BN, KC, NW, NX, ATMEM, NCONV, NISS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -171,8 +176,8 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
     uint64_t* xfree = afull + NX;
     uint64_t* accfull = xfree + NX;
     uint64_t* accempty = accfull + 2;
-    uint64_t* drain = accempty + 2;
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* drain = accempty + 2;                 // one per MMA issuer
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain + 2);
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
     int* s_cnt = reinterpret_cast<int*>(s_tmem + 4);
     int* s_off = s_cnt + 256;
@@ -192,10 +197,11 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
             mbar_init(smem_u32(&xfree[i]), 1);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(smem_u32(&accfull[i]), 1);
+            mbar_init(smem_u32(&accfull[i]), NISS);
             mbar_init(smem_u32(&accempty[i]), 4);
         }
-        mbar_init(smem_u32(drain), 1);
+        mbar_init(smem_u32(&drain[0]), 1);
+        mbar_init(smem_u32(&drain[1]), 1);
         fence_mbar_init();
         *s_abort = 0;
     }
@@ -293,11 +299,17 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                         mbar_wait(smem_u32(&fullb[i]), (last_par >> i) & 1u);
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == 1 || (NISS == 2 && warp == 3)) {
+        // ------------------------------------------------------------ MMA issuers
+        // One thread issues tcgen05.mma at a bounded rate; with NISS = 2 a
+        // second thread (warp 3) takes every other stage into its own partial
+        // accumulator, which nearly doubles the MMA issue rate for the narrow
+        // (few-token) tiles of decoding.
         if (lane == 0) {
+            const int me = (warp == 1) ? 0 : 1;
             int x = 0;
             uint32_t ph = 0;
+            uint32_t g = 0;
             int it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
@@ -311,30 +323,35 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t dt = tmem + static_cast<uint32_t>(d * BN);
-                for (int kb = 0; kb < p.kblocks; ++kb) {
-                    if (!mbar_wait_or_abort(smem_u32(&afull[x]), ph, s_abort)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint8_t* st = xring + x * Tr::kXBytes;
-                    const uint64_t bd0 = desc_kmajor_sw128(smem_u32(st));
-                    const uint64_t ad0 = ATMEM ? 0 : desc_kmajor_sw128(smem_u32(st + Tr::kBBytes));
-#pragma unroll
-                    for (int kk = 0; kk < KC / 32; ++kk) {
-                        const int atom = kk >> 2, sub = kk & 3;
-                        // start-address field advances in 16-byte units
-                        const uint64_t bd = bd0 + static_cast<uint64_t>((atom * BN * 128 + sub * 32) >> 4);
-                        const uint32_t acc = (kb | kk) ? 1u : 0u;
-                        if (ATMEM) {
-                            umma_f8_ta(dt, tmem_a + static_cast<uint32_t>(x * Tr::kACols + kk * 8), bd, idesc, acc);
-                        } else {
-                            const uint64_t ad = ad0 + static_cast<uint64_t>((atom * 128 * 128 + sub * 32) >> 4);
-                            umma_f8(dt, ad, bd, idesc, acc);
+                const uint32_t dt = tmem + static_cast<uint32_t>((d * NISS + me) * BN);
+                bool first = true;
+                for (int kb = 0; kb < p.kblocks; ++kb, ++g) {
+                    if (static_cast<int>(g % NISS) == me) {
+                        if (!mbar_wait_or_abort(smem_u32(&afull[x]), ph, s_abort)) {
+                            ok = false;
+                            break;
                         }
+                        tc_fence_after();
+                        const uint8_t* st = xring + x * Tr::kXBytes;
+                        const uint64_t bd0 = desc_kmajor_sw128(smem_u32(st));
+                        const uint64_t ad0 = ATMEM ? 0 : desc_kmajor_sw128(smem_u32(st + Tr::kBBytes));
+#pragma unroll
+                        for (int kk = 0; kk < KC / 32; ++kk) {
+                            const int atom = kk >> 2, sub = kk & 3;
+                            // start-address field advances in 16-byte units
+                            const uint64_t bd = bd0 + static_cast<uint64_t>((atom * BN * 128 + sub * 32) >> 4);
+                            const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+                            if (ATMEM) {
+                                umma_f8_ta(dt, tmem_a + static_cast<uint32_t>(x * Tr::kACols + kk * 8), bd, idesc,
+                                           acc);
+                            } else {
+                                const uint64_t ad = ad0 + static_cast<uint64_t>((atom * 128 * 128 + sub * 32) >> 4);
+                                umma_f8(dt, ad, bd, idesc, acc);
+                            }
+                        }
+                        first = false;
+                        umma_commit(smem_u32(&xfree[x]));
                     }
-                    umma_commit(smem_u32(&xfree[x]));
                     if (++x == NX) {
                         x = 0;
                         ph ^= 1u;
@@ -342,12 +359,12 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                 }
                 if (!ok)
                     break;
-                umma_commit(smem_u32(&accfull[d]));
+                umma_commit(smem_u32(&accfull[d]));   // (an issuer with no stage in this tile arrives at once)
             }
             if (!ok) {
                 fail();
-                umma_commit(smem_u32(drain));  // wait for MMAs in flight before TMEM goes away
-                mbar_wait(smem_u32(drain), 0);
+                umma_commit(smem_u32(&drain[me]));  // wait for MMAs in flight before TMEM goes away
+                mbar_wait(smem_u32(&drain[me]), 0);
             }
         }
     } else if (warp >= 4 && warp < Tr::kEpi0) {
@@ -437,6 +454,7 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
         const int q = warp & 3;
         const float a1 = __ldg(p.a1);
         const float a2 = __ldg(p.a2);
+        uint32_t gsum = 0;   // global stage index of the tile's first stage
         int it = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
@@ -449,9 +467,28 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
             }
             tc_fence_after();
             const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) +
-                                   static_cast<uint32_t>(d * BN);
+                                   static_cast<uint32_t>(d * NISS * BN);
+            // partial sum of issuer i is valid when the issuer had a stage in
+            // this tile: always when the tile has two or more stages
+            const bool v0 = NISS == 1 || p.kblocks >= 2 || (gsum % NISS) == 0;
+            const bool v1 = NISS == 2 && (p.kblocks >= 2 || (gsum % NISS) == 1);
+            gsum += p.kblocks;
             auto load_acc = [&](int c, uint32_t (&v)[32]) {
-                tmem_ld32(tbase + c, v);
+                if (v0) {
+                    tmem_ld32(tbase + c, v);
+                } else {
+#pragma unroll
+                    for (int xx = 0; xx < 32; ++xx)
+                        v[xx] = 0u;
+                }
+                if (v1) {
+                    uint32_t w2[32];
+                    tmem_ld32(tbase + BN + c, w2);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int xx = 0; xx < 32; ++xx)
+                        v[xx] = __float_as_uint(__uint_as_float(v[xx]) + __uint_as_float(w2[xx]));
+                }
                 tmem_ld_wait();
             };
             const int nchunks = (ti.ntok + 31) >> 5;
@@ -538,39 +575,44 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
 // unpack8); s0x[pos] = sum_h 512*dec(x) (exact);
 // s0h[pos] = 0 (the gate_up epilogue accumulates into it).
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) moe_gather_kernel(const uint8_t* __restrict__ xq, int H, int k,
+__global__ void __launch_bounds__(128) moe_gather_kernel(const uint8_t* __restrict__ xq, int H, int k,
                                                          const int32_t* __restrict__ sorted_ids,
                                                          int A, uint8_t* __restrict__ xp,
                                                          long long* __restrict__ s0x,
                                                          unsigned long long* __restrict__ s0h)
 {
-    const int lane = threadIdx.x & 31;
-    const int pos = blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (pos >= A)
-        return;
+    // one block per assignment row: every 16-byte chunk of the row is in
+    // flight at once
+    __shared__ long long red[4];
+    const int pos = blockIdx.x;
     const int t = __ldg(sorted_ids + pos) / k;
     const uint4* src = reinterpret_cast<const uint4*>(xq + static_cast<int64_t>(t) * H);
     uint4* dst = reinterpret_cast<uint4*>(xp + static_cast<int64_t>(pos) * H);
-    long long sum = 0;
-    for (int c = lane; c < H / 16; c += 32) {
+    int s = 0;
+    for (int c = threadIdx.x; c < H / 16; c += blockDim.x) {
         const uint4 v = __ldg(src + c);
         // permuted K order inside each group of 8 (see unpack8)
         dst[c] = make_uint4(prmt(v.x, v.y, 0x6420u), prmt(v.x, v.y, 0x7531u), prmt(v.z, v.w, 0x6420u),
                             prmt(v.z, v.w, 0x7531u));
         const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-        int s = 0;
 #pragma unroll
         for (int j = 0; j < 4; ++j)
 #pragma unroll
             for (int b = 0; b < 4; ++b)
                 s += e4m3_times512((u[j] >> (8 * b)) & 0xFFu);
-        sum += s;
     }
+    long long sum = s;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
         sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
-    if (lane == 0) {
-        s0x[pos] = sum;
+    if ((threadIdx.x & 31) == 0)
+        red[threadIdx.x >> 5] = sum;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        long long total = 0;
+        for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w)
+            total += red[w];
+        s0x[pos] = total;
         s0h[pos] = 0ull;
     }
 }
@@ -653,12 +695,7 @@ MoeConfig moe_pick_config(int T, int H, int I, int E, int k, int num_sms)
 {
     MoeConfig c;
     c.bn = pick_bn(T);
-    // stage depth along K: longer stages amortize the per-stage barrier work
-    // of the single MMA thread; the decode tile takes 512 when H and I allow
-    if (c.bn == 32 && H % 512 == 0 && I % 512 == 0)
-        c.kc = 512;
-    else
-        c.kc = (c.bn <= 128) ? 256 : 128;
+    c.kc = (c.bn <= 128) ? 256 : 128;
     // split the down projection's K so that its tiles fill the SMs evenly
     const int kblocks = I / c.kc;
     const int base_tiles = E * (H / 128);
@@ -680,12 +717,12 @@ MoeConfig moe_pick_config(int T, int H, int I, int E, int k, int num_sms)
     return c;
 }
 
-template <int MODE, int BN, int KC, int NW, int NX, bool ATMEM, int NCONV>
+template <int MODE, int BN, int KC, int NW, int NX, bool ATMEM, int NCONV, int NISS>
 static int launch_gemm(const CUtensorMap& tw, const CUtensorMap& tb, const MoeGemmParams& prm, int grid,
                        cudaStream_t s)
 {
-    using Tr = MoeTraits<MODE, BN, KC, NW, NX, ATMEM, NCONV>;
-    auto kern = moe_gemm_kernel<MODE, BN, KC, NW, NX, ATMEM, NCONV>;
+    using Tr = MoeTraits<MODE, BN, KC, NW, NX, ATMEM, NCONV, NISS>;
+    auto kern = moe_gemm_kernel<MODE, BN, KC, NW, NX, ATMEM, NCONV, NISS>;
     // attribute set on every launch: cheap, and correct for every device
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Tr::kSmem) != cudaSuccess)
         return kErrLaunch;
@@ -702,13 +739,10 @@ static int dispatch_gemm(const MoeConfig& cfg, const CUtensorMap& tw, const CUte
                          const MoeGemmParams& prm, int grid, cudaStream_t s)
 {
     switch (cfg.bn) {
-    case 32:
-        if (cfg.kc == 512)
-            return launch_gemm<MODE, 32, 512, 5, 3, true, 4>(tw, tb, prm, grid, s);
-        return launch_gemm<MODE, 32, 256, 10, 6, true, 4>(tw, tb, prm, grid, s);
-    case 64: return launch_gemm<MODE, 64, 256, 8, 4, true, 8>(tw, tb, prm, grid, s);
-    case 128: return launch_gemm<MODE, 128, 256, 4, 4, true, 8>(tw, tb, prm, grid, s);
-    default: return launch_gemm<MODE, 256, 128, 8, 3, false, 4>(tw, tb, prm, grid, s);
+    case 32: return launch_gemm<MODE, 32, 256, 10, 6, true, 8, 2>(tw, tb, prm, grid, s);
+    case 64: return launch_gemm<MODE, 64, 256, 8, 4, true, 8, 2>(tw, tb, prm, grid, s);
+    case 128: return launch_gemm<MODE, 128, 256, 4, 4, true, 8, 1>(tw, tb, prm, grid, s);
+    default: return launch_gemm<MODE, 256, 128, 8, 3, false, 4, 1>(tw, tb, prm, grid, s);
     }
 }
 
@@ -717,7 +751,7 @@ int launch_moe_forward(const MoeLaunch& L, const MoeConfig& cfg, int num_sms, cu
     const int A = L.T * L.k;
     const int BN = cfg.bn, KC = cfg.kc;
     // activations: gather + exact per-token sums
-    moe_gather_kernel<<<(A + 7) / 8, 256, 0, s>>>(L.xq, L.H, L.k, L.sorted_ids, A, L.xp, L.s0x, L.s0h);
+    moe_gather_kernel<<<A, 128, 0, s>>>(L.xq, L.H, L.k, L.sorted_ids, A, L.xp, L.s0x, L.s0h);
     if (cudaGetLastError() != cudaSuccess)
         return kErrLaunch;
 
