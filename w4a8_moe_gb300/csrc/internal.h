@@ -7,7 +7,29 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace w4a8 {
+
+// Launch `kern` as a programmatic dependent of the previous kernel in the
+// stream: it may start (and run its prologue) while that kernel finishes; it
+// executes griddepcontrol.wait before touching the predecessor's output.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // ---- quant.cu
 cudaError_t launch_quantize_experts(const uint16_t* w, int E, int N, int K, int32_t* packed,

@@ -205,6 +205,19 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
         fence_mbar_init();
         *s_abort = 0;
     }
+    grid_dep_launch();
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tm_w);
+        prefetch_tmap(&tm_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(s_tmem), Tr::kTmemCols);
+        tmem_relinquish();
+    }
+    // Everything above overlaps the previous kernel's tail. The routing
+    // counts, the activation operand and the buffers this kernel writes all
+    // belong to earlier kernels of the stream, so every thread waits here.
+    grid_dep_wait();
     if (threadIdx.x == 64) {
         int acc = 0;
         for (int e = 0; e < p.E; ++e) {
@@ -215,14 +228,6 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
             acc += p.rt_count * ((c + BN - 1) / BN) * p.ksplit;
         }
         s_pre[p.E] = acc;
-    }
-    if (warp == 0 && lane == 0) {
-        prefetch_tmap(&tm_w);
-        prefetch_tmap(&tm_b);
-    }
-    if (warp == 1) {
-        tmem_alloc(smem_u32(s_tmem), Tr::kTmemCols);
-        tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
@@ -584,6 +589,8 @@ __global__ void __launch_bounds__(128) moe_gather_kernel(const uint8_t* __restri
     // one block per assignment row: every 16-byte chunk of the row is in
     // flight at once
     __shared__ long long red[4];
+    grid_dep_launch();
+    grid_dep_wait();
     const int pos = blockIdx.x;
     const int t = __ldg(sorted_ids + pos) / k;
     const uint4* src = reinterpret_cast<const uint4*>(xq + static_cast<int64_t>(t) * H);
@@ -627,6 +634,8 @@ __global__ void __launch_bounds__(256) moe_finalize_kernel(
     const float* __restrict__ ypart, const unsigned long long* __restrict__ s0h,
     const float* __restrict__ s_d, const float* __restrict__ a2p, uint16_t* __restrict__ out)
 {
+    grid_dep_launch();
+    grid_dep_wait();
     const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int per_row = H / 4;
     if (idx >= static_cast<int64_t>(T) * per_row)
@@ -726,8 +735,9 @@ static int launch_gemm(const CUtensorMap& tw, const CUtensorMap& tb, const MoeGe
     // attribute set on every launch: cheap, and correct for every device
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Tr::kSmem) != cudaSuccess)
         return kErrLaunch;
-    kern<<<grid, Tr::kThreads, Tr::kSmem, s>>>(tw, tb, prm);
-    return cudaGetLastError() == cudaSuccess ? kOK : kErrLaunch;
+    return launch_dependent(kern, dim3(grid), dim3(Tr::kThreads), Tr::kSmem, s, tw, tb, prm) == cudaSuccess
+               ? kOK
+               : kErrLaunch;
 }
 
 // Token tile -> pipeline shape. Up to 128 tokens the unpacked weights live in
@@ -751,8 +761,8 @@ int launch_moe_forward(const MoeLaunch& L, const MoeConfig& cfg, int num_sms, cu
     const int A = L.T * L.k;
     const int BN = cfg.bn, KC = cfg.kc;
     // activations: gather + exact per-token sums
-    moe_gather_kernel<<<A, 128, 0, s>>>(L.xq, L.H, L.k, L.sorted_ids, A, L.xp, L.s0x, L.s0h);
-    if (cudaGetLastError() != cudaSuccess)
+    if (launch_dependent(moe_gather_kernel, dim3(A), dim3(128), 0, s, L.xq, L.H, L.k, L.sorted_ids, A, L.xp,
+                         L.s0x, L.s0h) != cudaSuccess)
         return kErrLaunch;
 
     // weight boxes: 64-byte rows (64-byte swizzle) for KC = 128, else 128-byte rows
@@ -819,9 +829,9 @@ int launch_moe_forward(const MoeLaunch& L, const MoeConfig& cfg, int num_sms, cu
     mark(2);
 
     const int64_t nthreads = static_cast<int64_t>(L.T) * (L.H / 4);
-    moe_finalize_kernel<<<static_cast<unsigned>((nthreads + 255) / 256), 256, 0, s>>>(
-        L.T, L.H, L.k, A, cfg.ksplit, L.ids, L.topk_w, L.inv, L.ypart, L.s0h, L.s_d, L.a2, L.out);
-    if (cudaGetLastError() != cudaSuccess)
+    if (launch_dependent(moe_finalize_kernel, dim3(static_cast<unsigned>((nthreads + 255) / 256)), dim3(256), 0, s,
+                         L.T, L.H, L.k, A, cfg.ksplit, L.ids, L.topk_w, L.inv, L.ypart,
+                         static_cast<const unsigned long long*>(L.s0h), L.s_d, L.a2, L.out) != cudaSuccess)
         return kErrLaunch;
     mark(3);
     return kOK;

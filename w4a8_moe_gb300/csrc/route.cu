@@ -99,6 +99,8 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
                                                          int32_t* __restrict__ ids,
                                                          float* __restrict__ w)
 {
+    grid_dep_launch();
+    grid_dep_wait();
     const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (t < T)
         route_token(logits, t, E, k, renorm, ids, w, nullptr);
@@ -108,6 +110,8 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
 __global__ void __launch_bounds__(256) route_hist_kernel(const int32_t* __restrict__ ids, int A,
                                                          int E, int32_t* __restrict__ block_hist)
 {
+    grid_dep_launch();
+    grid_dep_wait();
     __shared__ int cnt[kMaxE];
     for (int e = threadIdx.x; e < E; e += blockDim.x)
         cnt[e] = 0;
@@ -129,6 +133,8 @@ __global__ void __launch_bounds__(256) route_scan_kernel(const int32_t* __restri
                                                          int32_t* __restrict__ offsets,
                                                          int32_t* __restrict__ block_base)
 {
+    grid_dep_launch();
+    grid_dep_wait();
     __shared__ int tot[kMaxE];
     __shared__ int off[kMaxE + 1];
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -208,6 +214,8 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(const int32_t* __res
                                                             int32_t* __restrict__ sorted_ids,
                                                             int32_t* __restrict__ inv)
 {
+    grid_dep_launch();
+    grid_dep_wait();
     __shared__ int run[kMaxE];
     __shared__ int base[kMaxE];
     __shared__ int wcnt[8][kMaxE];
@@ -232,6 +240,8 @@ __global__ void __launch_bounds__(512) route_fused_kernel(const float* __restric
                                                            int32_t* __restrict__ sorted_ids,
                                                            int32_t* __restrict__ inv)
 {
+    grid_dep_launch();
+    grid_dep_wait();
     __shared__ int32_t s_ids[kRouteFusedMax];
     __shared__ int cnt[kMaxE];
     __shared__ int base[kMaxE];
@@ -268,17 +278,22 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, i
                          int32_t* inv, int32_t* block_hist, int32_t* block_base, cudaStream_t s)
 {
     const int A = T * k;
-    if (A <= kRouteFusedMax) {
-        route_fused_kernel<<<1, 512, 0, s>>>(logits, T, E, k, renorm, ids, w, counts, offsets,
-                                              sorted_ids, inv);
-        return cudaGetLastError();
-    }
+    if (A <= kRouteFusedMax)
+        return launch_dependent(route_fused_kernel, dim3(1), dim3(512), 0, s, logits, T, E, k, renorm, ids, w,
+                                counts, offsets, sorted_ids, inv);
     const int nb = (A + kRouteChunk - 1) / kRouteChunk;
-    route_topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(logits, T, E, k, renorm, ids, w);
-    route_hist_kernel<<<nb, 256, 0, s>>>(ids, A, E, block_hist);
-    route_scan_kernel<<<1, 256, 0, s>>>(block_hist, nb, E, A, counts, offsets, block_base);
-    route_scatter_kernel<<<nb, 256, 0, s>>>(ids, A, E, block_base, sorted_ids, inv);
-    return cudaGetLastError();
+    cudaError_t e = launch_dependent(route_topk_kernel, dim3((T + 7) / 8), dim3(256), 0, s, logits, T, E, k,
+                                     renorm, ids, w);
+    if (e == cudaSuccess)
+        e = launch_dependent(route_hist_kernel, dim3(nb), dim3(256), 0, s,
+                             static_cast<const int32_t*>(ids), A, E, block_hist);
+    if (e == cudaSuccess)
+        e = launch_dependent(route_scan_kernel, dim3(1), dim3(256), 0, s, static_cast<const int32_t*>(block_hist),
+                             nb, E, A, counts, offsets, block_base);
+    if (e == cudaSuccess)
+        e = launch_dependent(route_scatter_kernel, dim3(nb), dim3(256), 0, s, static_cast<const int32_t*>(ids), A,
+                             E, static_cast<const int32_t*>(block_base), sorted_ids, inv);
+    return e;
 }
 
 }  // namespace w4a8
