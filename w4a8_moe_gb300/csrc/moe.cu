@@ -137,12 +137,18 @@ __device__ __forceinline__ int kperm(int i)
     return (i & ~7) | ((i & 7) >> 1) | ((i & 1) << 2);
 }
 
-__device__ __forceinline__ float act_fn(float g, int act)
+// SiLU: z * sigmoid(z). GELU (tanh form): 0.5 z (1 + tanh(u)) with
+// u = sqrt(2/pi) (z + 0.044715 z^3), written as z * sigmoid(2u) (the same
+// function). The result is quantized to E4M3 next (3 mantissa bits), so the
+// error of the fast exponential and reciprocal is far below that rounding step.
+__device__ __forceinline__ float act_fn(float z, int act)
 {
-    if (act == 0)
-        return __fdiv_rn(g, 1.0f + expf(-g));
-    const float c = 0.7978845608028654f;  // sqrt(2/pi)
-    return 0.5f * g * (1.0f + tanhf(c * (g + 0.044715f * g * g * g)));
+    float t = -z;
+    if (act != 0) {
+        const float c2 = 1.5957691216057308f;  // 2 sqrt(2/pi)
+        t = -c2 * fmaf(0.044715f * z, z * z, z);
+    }
+    return __fdividef(z, 1.0f + __expf(t));
 }
 
 // Two rings, both indexed by the global stage number g of this CTA.
@@ -458,7 +464,7 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;
         const float a1 = __ldg(p.a1);
-        const float a2 = __ldg(p.a2);
+        const float inv_a2 = 1.0f / __ldg(p.a2);
         uint32_t gsum = 0;   // global stage index of the tile's first stage
         int it = 0;
         bool ok = true;
@@ -521,7 +527,7 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                             const float G = fmaf(512.0f, pg, -shift);
                             const float U = fmaf(512.0f, pu, -shift);
                             const float h = act_fn(sg * G, p.act) * (su * U);
-                            const uint32_t code = cvt_e4m3(__fdiv_rn(h, a2));
+                            const uint32_t code = cvt_e4m3(h * inv_a2);
                             p.hq[static_cast<int64_t>(pos) * p.I + kperm(i)] = static_cast<uint8_t>(code);
                             s512[cc] = e4m3_times512(code);
                         }
