@@ -509,8 +509,14 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                 const float sg = a1 * __ldg(p.s_gu + static_cast<int64_t>(ti.e) * 2 * p.I + i);
                 const float su = a1 * __ldg(p.s_gu + static_cast<int64_t>(ti.e) * 2 * p.I + p.I + i);
                 for (int ch = 0; ch < nchunks; ++ch) {
+                    // lane l fetches the exact shift of column ch*32 + l up front
+                    // (the loop below hands it around by shuffle), so no load
+                    // waits behind the byte stores of the loop
+                    const int mycol = ch * 32 + lane;
+                    const long long my_s0x = (mycol < ti.ntok) ? __ldg(p.s0x + ti.tok0 + mycol) : 0LL;
                     uint32_t v[32];
                     load_acc(ch * 32, v);
+                    const float my_shift = static_cast<float>(my_s0x) * (1.0f / 64.0f);
                     int s512[16];
 #pragma unroll
                     for (int cc = 0; cc < 16; ++cc) {
@@ -520,10 +526,10 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                         const float pg = half ? recv : __uint_as_float(v[cc]);
                         const float pu = half ? __uint_as_float(v[cc + 16]) : recv;
                         const int col = ch * 32 + cc + 16 * half;
+                        const float shift = __shfl_sync(0xFFFFFFFFu, my_shift, cc + 16 * half);
                         s512[cc] = 0;
                         if (col < ti.ntok) {
                             const int pos = ti.tok0 + col;
-                            const float shift = static_cast<float>(p.s0x[pos]) * (1.0f / 64.0f);
                             const float G = fmaf(512.0f, pg, -shift);
                             const float U = fmaf(512.0f, pu, -shift);
                             const float h = act_fn(sg * G, p.act) * (su * U);
