@@ -50,6 +50,8 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, i
                          int32_t* inv, int32_t* block_hist, int32_t* block_base, cudaStream_t s);
 
 // ---- moe.cu
+constexpr int kMaxKsplit = 16;   // largest split of the down projection's K
+
 struct MoeConfig {
     int bn;        // token tile (MMA N upper bound)
     int kc;        // K elements per pipeline stage

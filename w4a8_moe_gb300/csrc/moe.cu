@@ -661,17 +661,25 @@ __global__ void __launch_bounds__(256) moe_finalize_kernel(
         const int pos = __ldg(inv + a);
         const int e = __ldg(ids + a);
         const float wt = __ldg(topk_w + a);
-        float4 P = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int s = 0; s < ksplit; ++s) {
-            const float4 v =
-                __ldg(reinterpret_cast<const float4*>(ypart + (static_cast<int64_t>(s) * A + pos) * H + n));
-            P.x += v.x;
-            P.y += v.y;
-            P.z += v.z;
-            P.w += v.w;
-        }
+        // all split partials (at most kMaxKsplit) are requested before the
+        // first one is added, then summed in split order
+        float4 v[kMaxKsplit];
+#pragma unroll
+        for (int s = 0; s < kMaxKsplit; ++s)
+            if (s < ksplit)
+                v[s] = __ldg(reinterpret_cast<const float4*>(ypart + (static_cast<int64_t>(s) * A + pos) * H + n));
         const float shift = static_cast<float>(static_cast<long long>(__ldg(s0h + pos))) * (1.0f / 64.0f);
         const float4 sd = __ldg(reinterpret_cast<const float4*>(s_d + static_cast<int64_t>(e) * H + n));
+        float4 P = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int s = 0; s < kMaxKsplit; ++s) {
+            if (s < ksplit) {
+                P.x += v[s].x;
+                P.y += v[s].y;
+                P.z += v[s].z;
+                P.w += v[s].w;
+            }
+        }
         const float Pv[4] = {P.x, P.y, P.z, P.w};
         const float Sv[4] = {sd.x, sd.y, sd.z, sd.w};
 #pragma unroll
@@ -695,7 +703,7 @@ int moe_ksplit_max(int T, int k)
 {
     const int64_t A = static_cast<int64_t>(T) * k;
     if (A <= 128)
-        return 16;
+        return kMaxKsplit;
     if (A <= 1024)
         return 4;
     return 1;
@@ -717,20 +725,22 @@ MoeConfig moe_pick_config(int T, int H, int I, int E, int k, int num_sms)
     MoeConfig c;
     c.bn = pick_bn(T);
     c.kc = (c.bn <= 128) ? 256 : 128;
-    // split the down projection's K so that its tiles fill the SMs evenly
+    // Split the down projection's K so that its tiles fill the SMs: the cost
+    // of a split d is waves(d) * (stages per tile + a fixed per-tile cost of
+    // about one stage: the accumulator hand-off and the epilogue tail).
     const int kblocks = I / c.kc;
     const int base_tiles = E * (H / 128);
     const int kmax = moe_ksplit_max(T, k);
     int best = 1;
-    double best_eff = 0.0;
+    double best_cost = 0.0;
     for (int d = 1; d <= kmax; ++d) {
         if (kblocks % d != 0 || kblocks / d < 2)
             continue;
         const int64_t tiles = static_cast<int64_t>(base_tiles) * d;
         const int64_t waves = (tiles + num_sms - 1) / num_sms;
-        const double eff = static_cast<double>(tiles) / static_cast<double>(waves * num_sms);
-        if (eff > best_eff + 0.02) {
-            best_eff = eff;
+        const double cost = static_cast<double>(waves) * (static_cast<double>(kblocks / d) + 1.0);
+        if (d == 1 || cost < best_cost) {
+            best_cost = cost;
             best = d;
         }
     }
