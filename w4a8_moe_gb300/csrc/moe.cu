@@ -211,7 +211,6 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
         fence_mbar_init();
         *s_abort = 0;
     }
-    grid_dep_launch();
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tm_w);
         prefetch_tmap(&tm_b);
@@ -220,10 +219,13 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
         tmem_alloc(smem_u32(s_tmem), Tr::kTmemCols);
         tmem_relinquish();
     }
-    // Everything above overlaps the previous kernel's tail. The routing
-    // counts, the activation operand and the buffers this kernel writes all
-    // belong to earlier kernels of the stream, so every thread waits here.
-    grid_dep_wait();
+    // Programmatic launch: every kernel of the forward chain lets its
+    // dependents launch only after its own griddepcontrol.wait returned, so
+    // when this kernel runs, every kernel before its immediate predecessor has
+    // completed -- in particular the router that wrote counts and offsets.
+    // Those are read here without waiting, and the weight stream (which no
+    // kernel writes) starts at once; only the activation producer and the
+    // epilogue, which read or overwrite the predecessor's buffers, wait.
     if (threadIdx.x == 64) {
         int acc = 0;
         for (int e = 0; e < p.E; ++e) {
@@ -252,6 +254,10 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
         // warp 0: packed weights into the W ring; warp 2: activations into the X ring
         if (lane == 0) {
             const bool wprod = (warp == 0);
+            if (!wprod) {
+                grid_dep_wait();
+                grid_dep_launch();
+            }
             const int nslot = wprod ? NW : NX;
             uint64_t* fullb = wprod ? wfull : bfull;
             uint64_t* freeb = wprod ? wfree : xfree;
@@ -463,6 +469,8 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
     } else if (warp >= Tr::kEpi0) {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;
+        grid_dep_wait();
+        grid_dep_launch();
         const float a1 = __ldg(p.a1);
         const float inv_a2 = 1.0f / __ldg(p.a2);
         uint32_t gsum = 0;   // global stage index of the tile's first stage
@@ -601,8 +609,8 @@ __global__ void __launch_bounds__(128) moe_gather_kernel(const uint8_t* __restri
     // one block per assignment row: every 16-byte chunk of the row is in
     // flight at once
     __shared__ long long red[4];
-    grid_dep_launch();
     grid_dep_wait();
+    grid_dep_launch();
     const int pos = blockIdx.x;
     const int t = __ldg(sorted_ids + pos) / k;
     const uint4* src = reinterpret_cast<const uint4*>(xq + static_cast<int64_t>(t) * H);
@@ -646,8 +654,8 @@ __global__ void __launch_bounds__(256) moe_finalize_kernel(
     const float* __restrict__ ypart, const unsigned long long* __restrict__ s0h,
     const float* __restrict__ s_d, const float* __restrict__ a2p, uint16_t* __restrict__ out)
 {
-    grid_dep_launch();
     grid_dep_wait();
+    grid_dep_launch();
     const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int per_row = H / 4;
     if (idx >= static_cast<int64_t>(T) * per_row)

@@ -99,8 +99,8 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
                                                          int32_t* __restrict__ ids,
                                                          float* __restrict__ w)
 {
-    grid_dep_launch();
     grid_dep_wait();
+    grid_dep_launch();
     const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (t < T)
         route_token(logits, t, E, k, renorm, ids, w, nullptr);
@@ -110,8 +110,8 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
 __global__ void __launch_bounds__(256) route_hist_kernel(const int32_t* __restrict__ ids, int A,
                                                          int E, int32_t* __restrict__ block_hist)
 {
-    grid_dep_launch();
     grid_dep_wait();
+    grid_dep_launch();
     __shared__ int cnt[kMaxE];
     for (int e = threadIdx.x; e < E; e += blockDim.x)
         cnt[e] = 0;
@@ -133,8 +133,8 @@ __global__ void __launch_bounds__(256) route_scan_kernel(const int32_t* __restri
                                                          int32_t* __restrict__ offsets,
                                                          int32_t* __restrict__ block_base)
 {
-    grid_dep_launch();
     grid_dep_wait();
+    grid_dep_launch();
     __shared__ int tot[kMaxE];
     __shared__ int off[kMaxE + 1];
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -214,8 +214,8 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(const int32_t* __res
                                                             int32_t* __restrict__ sorted_ids,
                                                             int32_t* __restrict__ inv)
 {
-    grid_dep_launch();
     grid_dep_wait();
+    grid_dep_launch();
     __shared__ int run[kMaxE];
     __shared__ int base[kMaxE];
     __shared__ int wcnt[8][kMaxE];
@@ -240,8 +240,8 @@ __global__ void __launch_bounds__(512) route_fused_kernel(const float* __restric
                                                            int32_t* __restrict__ sorted_ids,
                                                            int32_t* __restrict__ inv)
 {
-    grid_dep_launch();
     grid_dep_wait();
+    grid_dep_launch();
     __shared__ int32_t s_ids[kRouteFusedMax];
     __shared__ int cnt[kMaxE];
     __shared__ int base[kMaxE];
