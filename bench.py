@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--cpu-sample-tokens", type=int, default=0,
                     help="tokens in the oracle sample (0: sized for ~15 s of CPU work)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--suite", action="store_true",
+                    help="also print one line per secondary workload (Grok-1 layers, block-FP8)")
     return ap.parse_args()
 
 
@@ -81,6 +83,11 @@ def max_over_ranks(x: float, world: int) -> float:
     t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def throughput(world: int, tokens_per_rank: int, steps: int, ms_slowest: float) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank * steps / (ms_slowest / 1e3)
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -171,6 +178,86 @@ def static_hidden_scale(inp, shape, tokens=8):
     return hmax / 448.0 if hmax > 0 else 1.0
 
 
+def prepare_moe(shape, seed, dev):
+    """Seeded synthetic layer: packed weights, calibrated static scales, routing."""
+    import torch
+
+    import w4a8_moe_gb300 as lib
+    from w4a8_moe_gb300 import synth
+
+    inp = synth.moe_inputs(shape.T, shape.H, shape.I, shape.E, bias_std=shape.bias_std,
+                           seed=seed, device=dev)
+    w_gu, s_gu = lib.w4a8_quantize_experts(inp["w_gu"])
+    w_d, s_d = lib.w4a8_quantize_experts(inp["w_d"])
+    xq, a1 = lib.w4a8_quantize_act(inp["x"], compute_scale=True)      # calibration of a1
+    s2 = static_hidden_scale(inp, shape)
+    a2 = torch.tensor([s2], dtype=torch.float32, device=dev)
+    st = {"w_gu": w_gu, "s_gu": s_gu, "w_d": w_d, "s_d": s_d, "xq": xq, "a1": a1, "a2": a2,
+          "logits": inp["logits"], "x": inp["x"]}
+    del inp
+    torch.cuda.empty_cache()
+    T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
+    st["route_ws"] = torch.zeros(lib.moe_route_workspace_size(T, E, k), dtype=torch.uint8, device=dev)
+    st["ws"] = torch.zeros(lib.moe_w4a8_workspace_size(T, H, I, E, k), dtype=torch.uint8, device=dev)
+    st["out"] = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    st["route"] = lib.moe_route(st["logits"], k, ws=st["route_ws"])
+    return st
+
+
+def moe_step(lib, shape, st):
+    """One step of the hot path: route + forward, inputs resident on the device."""
+    lib.moe_route(st["logits"], shape.k, out=st["route"], ws=st["route_ws"])
+    lib.moe_w4a8_forward(st["xq"], st["a1"], st["w_gu"], st["s_gu"], st["w_d"], st["s_d"], st["a2"],
+                         shape.act, st["route"], out=st["out"], ws=st["ws"])
+
+
+def time_moe_steps(lib, shape, st, steps, warmup, world, clock_index=None):
+    """K timed steps between barriers, CUDA events on the launching stream.
+    Per-kernel events (recorded by the library around the two GEMMs and the
+    combine) go into every PROFILE_EVERY-th step only: an event between two
+    kernels stops the next one from launching early, so recording them in
+    every step would slow the step it measures."""
+    import torch
+
+    stream = torch.cuda.current_stream()
+    for _ in range(max(3, warmup)):
+        moe_step(lib, shape, st)
+    torch.cuda.synchronize()
+    counts = st["route"].counts.cpu().tolist()
+    sampled = list(range(0, steps, PROFILE_EVERY))
+    ev = {i: [torch.cuda.Event(enable_timing=True) for _ in range(4)] for i in sampled}
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for e4 in ev.values():  # materialize the CUDA events before the timed region
+        for e in e4:
+            e.record(stream)
+    barrier(world)
+    torch.cuda.synchronize()
+    clk = ClockSampler(clock_index if clock_index is not None else torch.cuda.current_device())
+    with clk:
+        start.record(stream)
+        for i in range(steps):
+            if i in ev:
+                lib.w4a8_set_profile_events(ev[i])
+                moe_step(lib, shape, st)
+                lib.w4a8_set_profile_events(None)
+            else:
+                moe_step(lib, shape, st)
+        stop.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms_total = max_over_ranks(start.elapsed_time(stop), world)
+    assert lib.w4a8_device_error(st["ws"]) == 0, "device error word set"
+    ms_gu = statistics.mean(e[0].elapsed_time(e[1]) for e in ev.values())
+    ms_dn = statistics.mean(e[1].elapsed_time(e[2]) for e in ev.values())
+    ms_fin = statistics.mean(e[2].elapsed_time(e[3]) for e in ev.values())
+    gu_bytes, d_bytes, act_bytes = algorithmic_bytes(shape, counts)
+    return {"ms_per_step": ms_total / steps, "clocks": clk.summary(),
+            "kernels": {"gate_up_ms": ms_gu, "down_ms": ms_dn, "finalize_ms": ms_fin,
+                        "route_gather_gaps_ms": ms_total / steps - ms_gu - ms_dn - ms_fin,
+                        "gate_up_bytes": gu_bytes, "down_bytes": d_bytes, "act_bytes": act_bytes,
+                        "active_experts": sum(1 for c in counts if c > 0)}}
+
+
 def run_ours(args, rank, world):
     import torch
 
@@ -179,83 +266,40 @@ def run_ours(args, rank, world):
 
     shape = synth.MOE_SHAPES[args.config]
     dev = torch.device("cuda", torch.cuda.current_device())
-    inp = synth.moe_inputs(shape.T, shape.H, shape.I, shape.E, bias_std=shape.bias_std,
-                           seed=rank, device=dev)
-    w_gu, s_gu = lib.w4a8_quantize_experts(inp["w_gu"])
-    w_d, s_d = lib.w4a8_quantize_experts(inp["w_d"])
-    xq, a1 = lib.w4a8_quantize_act(inp["x"], compute_scale=True)      # calibration of a1
-    s2 = static_hidden_scale(inp, shape)
-    a2 = torch.tensor([s2], dtype=torch.float32, device=dev)
-    logits = inp["logits"]
-    x_bf16 = inp["x"]
-    del inp["w_gu"], inp["w_d"]
-    torch.cuda.empty_cache()
+    st = prepare_moe(shape, rank, dev)
+    T, H, k = shape.T, shape.H, shape.k
+    tm = time_moe_steps(lib, shape, st, args.steps, args.warmup, world)
 
-    T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
-    route_ws = torch.zeros(lib.moe_route_workspace_size(T, E, k), dtype=torch.uint8, device=dev)
-    ws = torch.zeros(lib.moe_w4a8_workspace_size(T, H, I, E, k), dtype=torch.uint8, device=dev)
-    out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
-    route = lib.moe_route(logits, k, ws=route_ws)
-    stream = torch.cuda.current_stream()
-
-    def step():
-        lib.moe_route(logits, k, out=route, ws=route_ws)
-        lib.moe_w4a8_forward(xq, a1, w_gu, s_gu, w_d, s_d, a2, shape.act, route, out=out, ws=ws)
-
-    for _ in range(max(3, args.warmup)):
-        step()
+    # the static-scale activation quantization that precedes the layer,
+    # timed on its own (it is not part of the layer step)
+    n_aq = 200
+    for _ in range(5):
+        lib.w4a8_quantize_act(st["x"], scale=st["a1"], compute_scale=False, out=st["xq"])
+    s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s_ev.record()
+    for _ in range(n_aq):
+        lib.w4a8_quantize_act(st["x"], scale=st["a1"], compute_scale=False, out=st["xq"])
+    e_ev.record()
     torch.cuda.synchronize()
-    counts = route.counts.cpu().tolist()
-    gu_bytes, d_bytes, act_bytes = algorithmic_bytes(shape, counts)
-
-    # timed region: K steps between barriers, events on the launching stream.
-    # Per-kernel events (recorded by the library around the two GEMMs and the
-    # combine) go into every PROFILE_EVERY-th step only: an event between two
-    # kernels stops the next one from launching early, so recording them in
-    # every step would slow the step it measures.
-    sampled = list(range(0, args.steps, PROFILE_EVERY))
-    ev = {i: [torch.cuda.Event(enable_timing=True) for _ in range(4)] for i in sampled}
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    for e4 in ev.values():  # materialize the CUDA events before the timed region
-        for e in e4:
-            e.record(stream)
-    barrier(world)
-    torch.cuda.synchronize()
-    with ClockSampler(torch.cuda.current_device()) as clk:
-        start.record(stream)
-        for i in range(args.steps):
-            if i in ev:
-                lib.w4a8_set_profile_events(ev[i])
-                step()
-                lib.w4a8_set_profile_events(None)
-            else:
-                step()
-        stop.record(stream)
-        torch.cuda.synchronize()
-    barrier(world)
-    ms_total = start.elapsed_time(stop)
-    ms_total = max_over_ranks(ms_total, world)
-    ms_gu = statistics.mean(e[0].elapsed_time(e[1]) for e in ev.values())
-    ms_dn = statistics.mean(e[1].elapsed_time(e[2]) for e in ev.values())
-    ms_fin = statistics.mean(e[2].elapsed_time(e[3]) for e in ev.values())
-    assert lib.w4a8_device_error(ws) == 0, "device error word set"
+    act_quant_ms = s_ev.elapsed_time(e_ev) / n_aq
 
     # end to end through the public API with host buffers: H2D of the step's
     # inputs (bf16 x, fp32 logits) from pinned memory, static-scale quantization,
     # route, forward, D2H of the bf16 output
-    hx = x_bf16.cpu().pin_memory()
-    hl = logits.cpu().pin_memory()
+    hx = st["x"].cpu().pin_memory()
+    hl = st["logits"].cpu().pin_memory()
     hout = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
-    dx = torch.empty_like(x_bf16)
-    dl = torch.empty_like(logits)
+    dx = torch.empty_like(st["x"])
+    dl = torch.empty_like(st["logits"])
 
     def e2e_step():
         dx.copy_(hx, non_blocking=True)
         dl.copy_(hl, non_blocking=True)
-        lib.w4a8_quantize_act(dx, scale=a1, compute_scale=False, out=xq)
-        lib.moe_route(dl, k, out=route, ws=route_ws)
-        lib.moe_w4a8_forward(xq, a1, w_gu, s_gu, w_d, s_d, a2, shape.act, route, out=out, ws=ws)
-        hout.copy_(out, non_blocking=True)
+        lib.w4a8_quantize_act(dx, scale=st["a1"], compute_scale=False, out=st["xq"])
+        lib.moe_route(dl, k, out=st["route"], ws=st["route_ws"])
+        lib.moe_w4a8_forward(st["xq"], st["a1"], st["w_gu"], st["s_gu"], st["w_d"], st["s_d"], st["a2"],
+                             shape.act, st["route"], out=st["out"], ws=st["ws"])
+        hout.copy_(st["out"], non_blocking=True)
 
     for _ in range(max(3, args.warmup)):
         e2e_step()
@@ -268,21 +312,115 @@ def run_ours(args, rank, world):
         torch.cuda.synchronize()
     e2e_s = max_over_ranks(time.perf_counter() - t0, world)
 
-    res = {
-        "ms_per_step": ms_total / args.steps,
-        "value": world * T * args.steps / (ms_total / 1e3),
+    return {
+        "ms_per_step": tm["ms_per_step"],
+        "value": throughput(world, T, args.steps, tm["ms_per_step"] * args.steps),
         "e2e": {"value": world * T * e_steps / e2e_s, "unit": UNIT,
                 "h2d_bytes_per_step": hx.numel() * 2 + hl.numel() * 4,
                 "d2h_bytes_per_step": hout.numel() * 2},
-        "clocks": clk.summary(),
-        "kernels": {"gate_up_ms": ms_gu, "down_ms": ms_dn, "finalize_ms": ms_fin,
-                    "route_gather_gaps_ms": ms_total / args.steps - ms_gu - ms_dn - ms_fin,
-                    "gate_up_bytes": gu_bytes,
-                    "down_bytes": d_bytes, "act_bytes": act_bytes,
-                    "active_experts": sum(1 for c in counts if c > 0)},
+        "clocks": tm["clocks"],
+        "kernels": tm["kernels"],
+        "act_quant_static_ms": act_quant_ms,
         "shape": shape,
     }
-    return res
+
+
+def load_peaks():
+    pp = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    return json.load(open(pp)) if os.path.exists(pp) else {}
+
+
+def run_suite(args):
+    """Secondary workloads, one JSON line each (not the headline): the Grok-1
+    shaped layers (decode at 32, 8 and 1 tokens: weight GB/s against HBM;
+    prefill at 32768 tokens: FP8 TFLOP/s against the dense FP8 peak) and the
+    block-FP8 linear (GB/s at M <= 64, TFLOP/s at M = 4096)."""
+    import torch
+
+    import w4a8_moe_gb300 as lib
+    from w4a8_moe_gb300 import synth
+
+    peaks = load_peaks()
+    hbm = peaks.get("hbm_gbs", 6800.0)
+    # FP8 dense peak: the measured bf16 peak times the nominal fp8/bf16 ratio (2)
+    fp8_burst = 2.0 * peaks.get("bf16_tflops", 1900.0)
+    fp8_sust = 2.0 * peaks.get("bf16_tflops_sustained", 1700.0)
+    src = "MEASURED_PEAKS.json" if peaks else "fallback"
+    dev = torch.device("cuda", torch.cuda.current_device())
+    for name, steps, warm in (("grok_decode", 200, 10), ("grok_decode_t8", 200, 10),
+                              ("grok_decode_t1", 200, 10), ("grok_prefill", 6, 2)):
+        shape = synth.MOE_SHAPES[name]
+        st = prepare_moe(shape, 0, dev)
+        tm = time_moe_steps(lib, shape, st, steps, warm, 1)
+        kk = tm["kernels"]
+        ms = tm["ms_per_step"]
+        line = {"suite": True, "workload": shape.name, "ms_per_step": ms,
+                "tokens_per_s": shape.T / (ms * 1e-3), "steps": steps, "warmup": warm,
+                "kernels_ms": {"gate_up": kk["gate_up_ms"], "down": kk["down_ms"],
+                               "finalize": kk["finalize_ms"]},
+                "active_experts": kk["active_experts"], "clocks": tm["clocks"]}
+        wbytes = kk["gate_up_bytes"] + kk["down_bytes"] + kk["act_bytes"]
+        if shape.T <= 256:
+            gbs = wbytes / (ms * 1e-3) / 1e9
+            line.update({"bound": "hbm", "layer_gbs": gbs, "peak_gbs": hbm, "frac": gbs / hbm,
+                         "peak_source": src + " hbm_gbs"})
+        else:
+            flops = 2.0 * shape.T * shape.k * 3 * shape.H * shape.I
+            tf = flops / (ms * 1e-3) / 1e12
+            line.update({"bound": "tensor", "tflops": tf, "peak_tflops": fp8_sust,
+                         "frac": tf / fp8_sust,
+                         "peak_source": src + " bf16_tflops_sustained x 2 (nominal fp8/bf16)",
+                         "gate_up_tflops": 2.0 * shape.T * shape.k * 2 * shape.H * shape.I
+                         / (kk["gate_up_ms"] * 1e-3) / 1e12,
+                         "down_tflops": 2.0 * shape.T * shape.k * shape.H * shape.I
+                         / (kk["down_ms"] * 1e-3) / 1e12})
+        print(json.dumps(line), flush=True)
+        del st
+        torch.cuda.empty_cache()
+
+    # block-FP8 linear: four rotating weight copies (> L2) so that every call
+    # reads its weights from HBM
+    for (N, K) in synth.BLOCK_FP8_SHAPES:
+        ws_list, wsi_list = [], []
+        for c in range(4):
+            w = synth.block_fp8_inputs(1, N, K, seed=c, device=dev)["w"].float()
+            blk = w.view(N // 128, 128, K // 128, 128).abs().amax(dim=(1, 3))
+            wsi = torch.where(blk > 0, blk / 448.0, torch.ones_like(blk))
+            q = (w / wsi.repeat_interleave(128, 0).repeat_interleave(128, 1)).to(torch.float8_e4m3fn)
+            ws_list.append(q.view(torch.uint8).contiguous())
+            wsi_list.append(wsi.contiguous())
+            del w
+        for M in synth.BLOCK_FP8_M:
+            x = synth.block_fp8_inputs(M, N, K, seed=9, device=dev)["x"]
+            y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+            wsp = torch.zeros(lib.fp8_block_linear_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
+            iters = 400 if M <= 64 else 40
+            for i in range(8):
+                lib.fp8_block_linear(x, ws_list[i % 4], wsi_list[i % 4], out=y, ws=wsp)
+            torch.cuda.synchronize()
+            s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s_ev.record()
+            for i in range(iters):
+                lib.fp8_block_linear(x, ws_list[i % 4], wsi_list[i % 4], out=y, ws=wsp)
+            e_ev.record()
+            torch.cuda.synchronize()
+            assert lib.w4a8_device_error(wsp) == 0, "device error word set"
+            ms = s_ev.elapsed_time(e_ev) / iters
+            nbytes = N * K + 4 * (N // 128) * (K // 128) + 2 * M * K + 2 * M * N
+            flops = 2.0 * M * N * K
+            line = {"suite": True, "workload": f"block-FP8 linear N{N} K{K} M{M}", "ms_per_call": ms,
+                    "gbs": nbytes / (ms * 1e-3) / 1e9, "tflops": flops / (ms * 1e-3) / 1e12,
+                    "l2": "4 rotating weight copies"}
+            if M <= 64:
+                line.update({"bound": "hbm", "frac": line["gbs"] / hbm, "peak_gbs": hbm,
+                             "peak_source": src + " hbm_gbs"})
+            else:
+                line.update({"bound": "tensor", "frac": line["tflops"] / fp8_burst,
+                             "peak_tflops": fp8_burst,
+                             "peak_source": src + " bf16_tflops x 2 (nominal fp8/bf16)"})
+            print(json.dumps(line), flush=True)
+        del ws_list, wsi_list
+        torch.cuda.empty_cache()
 
 
 def cpu_baseline(args, shape):
@@ -359,10 +497,7 @@ def main():
     res = run_ours(args, rank, world)
     if rank != 0:
         return
-    peaks = {}
-    pp = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    if os.path.exists(pp):
-        peaks = json.load(open(pp))
+    peaks = load_peaks()
     hbm_peak = peaks.get("hbm_gbs", 6800.0)
     kk = res["kernels"]
     gu_gbs = kk["gate_up_bytes"] / (kk["gate_up_ms"] * 1e-3) / 1e9
@@ -384,10 +519,13 @@ def main():
             "layer_weight_gbs": layer_bytes / (res["ms_per_step"] * 1e-3) / 1e9,
             "layer_hbm_frac": layer_bytes / (res["ms_per_step"] * 1e-3) / 1e9 / hbm_peak,
             "roofline": roof, "e2e": res["e2e"], "clocks": res["clocks"],
-            "gpu_launches": 5 * args.steps}
+            "gpu_launches": 5 * args.steps,
+            "act_quant_static_ms": res["act_quant_static_ms"]}
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args, shape)
     print(json.dumps(line), flush=True)
+    if args.suite and world == 1:
+        run_suite(args)
 
 
 if __name__ == "__main__":
