@@ -85,6 +85,27 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
+# DRAM bytes (read + write) per launch of the GEMMs from one ncu capture of the
+# Mixtral decode layer (profiles/moe_gemm_mixtral_decode.md), valid only for
+# the GEMM sources they were taken on: a changed kernel reports null.
+NCU_TRAFFIC = {
+    "sources": ["w4a8_moe_gb300/csrc/moe.cu", "w4a8_moe_gb300/csrc/ptx.cuh",
+                "w4a8_moe_gb300/csrc/internal.h"],
+    "sha256": "5317ff6adc7bc811515948b2f29aee0b2182ee062074ee1a3b5f81f971169a91",
+    "gate_up": 470996736 + 4179200,
+    "down": 235840512 + 4016128,
+}
+
+
+def ncu_traffic(kernel: str):
+    import hashlib
+    h = hashlib.sha256()
+    for f in NCU_TRAFFIC["sources"]:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return NCU_TRAFFIC[kernel] if h.hexdigest() == NCU_TRAFFIC["sha256"] else None
+
+
 def throughput(world: int, tokens_per_rank: int, steps: int, ms_slowest: float) -> float:
     """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
     return world * tokens_per_rank * steps / (ms_slowest / 1e3)
@@ -504,9 +525,11 @@ def main():
     roof = {"bound": "hbm", "kernel": "moe_gemm_kernel<gate_up>", "achieved": gu_gbs,
             "peak": hbm_peak, "unit": "GB/s", "frac": gu_gbs / hbm_peak,
             "peak_source": "MEASURED_PEAKS.json hbm_gbs (burst copy)" if peaks else "fallback 6.8 TB/s",
-            "traffic": None,
+            "traffic": ncu_traffic("gate_up") if args.config == "mixtral_decode" else None,
+            "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
             "per_launch_ms": kk["gate_up_ms"], "algorithmic_bytes": kk["gate_up_bytes"],
             "down": {"per_launch_ms": kk["down_ms"], "algorithmic_bytes": kk["down_bytes"],
+                     "traffic": ncu_traffic("down") if args.config == "mixtral_decode" else None,
                      "achieved": kk["down_bytes"] / (kk["down_ms"] * 1e-3) / 1e9},
             "step_breakdown_ms": {"gate_up": kk["gate_up_ms"], "down": kk["down_ms"],
                                   "finalize": kk["finalize_ms"],
