@@ -10,7 +10,9 @@ N(0, 0.5)); --config selects another layer shape. Weights (705.7 MB packed for
 8 active experts) are far larger than L2, so every step streams them from HBM.
 
 Prints one JSON line (rank 0). `python bench.py --impl reference` times the CPU
-oracle on a bounded sample of the same workload instead.
+oracle on a bounded sample of the same workload instead. `--suite` adds one
+line per secondary workload (Grok-1-shaped layers, block-FP8 linear) after the
+headline line.
 
 Multi-GPU (torchrun): every rank runs its own replica of the layer on its own
 tokens (the path has no exchange step), timed between barriers; value is the
