@@ -135,6 +135,8 @@ struct BlkWs {
     float* xs_t;
     int ld_t;
     float* ypart;
+    int* tile_cnt;   // split-K counters, one per (128-row weight tile, token tile)
+    int n_cnt;
 };
 static size_t blk_ws(int M, int N, int K, BlkWs* w, void* ws)
 {
@@ -144,6 +146,9 @@ static size_t blk_ws(int M, int N, int K, BlkWs* w, void* ws)
     w->xs_t = c.take<float>(static_cast<size_t>(K / 128) * w->ld_t * 4);
     const int ks = blk_ksplit_max(M, K);
     w->ypart = c.take<float>(ks > 1 ? static_cast<size_t>(ks) * M * N * 4 : 0);
+    // token tiles are at least 16 wide
+    w->n_cnt = (N / 128) * ((M + 15) / 16);
+    w->tile_cnt = c.take<int>(static_cast<size_t>(w->n_cnt) * 4);
     return c.off;
 }
 
@@ -352,7 +357,7 @@ int fp8_block_linear(const uint16_t* x_bf16, int M, int N, int K, const uint8_t*
     BlkWs w;
     blk_ws(M, N, K, &w, ws);
     uint8_t* xq = xq_out ? xq_out : w.xq;
-    if (launch_block_act_quant(x_bf16, M, K, xq, xs_out, w.xs_t, w.ld_t, s) != cudaSuccess)
+    if (launch_block_act_quant(x_bf16, M, K, xq, xs_out, w.xs_t, w.ld_t, w.tile_cnt, w.n_cnt, s) != cudaSuccess)
         return W4A8_ERR_LAUNCH;
     BlkLaunch L{};
     L.M = M;
@@ -365,6 +370,7 @@ int fp8_block_linear(const uint16_t* x_bf16, int M, int N, int K, const uint8_t*
     L.xs_t = w.xs_t;
     L.ld_t = w.ld_t;
     L.ypart = w.ypart;
+    L.tile_cnt = w.tile_cnt;
     L.err = static_cast<uint32_t*>(ws);
     const BlkConfig cfg = blk_pick_config(M, N, K, sms);
     return launch_block_gemm(L, cfg, sms, s);

@@ -9,41 +9,76 @@
 // of 128 has its own pair of scales: the tensor cores produce the block's fp32
 // partial product in TMEM (4 MMAs of K = 32), and the epilogue warps fold it
 // into register accumulators as  acc += partial * xs[m, g] * Wsi[n/128, g].
-// Two TMEM partial buffers let the MMA of block g+1 overlap that fold.
+// NBUF TMEM partial buffers let the MMAs run up to NBUF K-blocks ahead of the
+// fold.
 //
-// Roles (12 warps): warp 0 TMA (weight tile 128x128, activation tile BNx128,
-// the BN activation scales of the block), warp 1 TMEM + MMA issuer, warps
-// 4-11 epilogue (two warps per 32-lane TMEM quadrant, each half of the BN
+// Roles (12 warps): warp 0 streams the weight tiles [128 x 128] (it starts
+// before the dependency wait: no kernel of the call writes the weights), warp 2
+// the activation tiles [BN x 128] and, into a ring of their own that only the
+// epilogue releases, the BN activation scales of each K-block; warp 1 owns TMEM
+// and issues the MMAs, whose commit alone frees a weight/activation slot;
+// warps 4-11 fold (two warps per 32-lane TMEM quadrant, each half of the BN
 // token columns). Swapped operands: M = 128 weight rows, N = BN tokens.
+//
+// When K is split over several CTAs, each writes its fp32 partial and bumps a
+// per-tile counter; the CTA that completes the count sums the partials in
+// split order and writes the bf16 tile (the counters are zeroed by the
+// activation-quantization kernel of the same call).
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace w4a8 {
+
+constexpr int kBlkMaxKsplit = 16;   // largest split of K
 
 struct BlkParams {
     int M, N, K, KB;
     int kb_per_split, ksplit, mt_count, nb_count;
     const float* wsi;   // [N/128, K/128]
     float* ypart;       // [ksplit, M, N] when ksplit > 1
+    int* tile_cnt;      // [nb_count * mt_count] when ksplit > 1, zero at entry
     uint16_t* y;        // [M, N]
     uint32_t* err;
 };
 
 template <int BN, int PST>
 struct BlkTraits {
-    static constexpr int kA = 128 * 128;
-    static constexpr int kB = BN * 128;
-    static constexpr int kS = ((BN * 4 + 1023) / 1024) * 1024;
-    static constexpr int kStage = kA + kB + kS;
-    static constexpr int kData = PST * kStage;
-    static constexpr int kBars = 2 * PST + 4 + 1;
-    static constexpr int kSmem = 1024 + kData + kBars * 8 + 16;
-    static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
+    static constexpr int kA = 128 * 128;                  // weight tile
+    static constexpr int kB = BN * 128;                   // activation tile
+    static constexpr int kStage = kA + kB;
+    static constexpr int kNbuf = (512 / BN) < 8 ? (512 / BN) : 8;   // TMEM partial buffers
+    static constexpr int kNs = PST + kNbuf;               // scale ring depth
+    static constexpr int kSBytes = BN * 4;                               // one scale slot's copy
+    static constexpr int kSStride = ((kSBytes + 127) / 128) * 128;       // TMA destinations: 128-byte aligned
+    static constexpr int kData = PST * kStage + ((kNs * kSStride + 1023) / 1024) * 1024;
+    static constexpr int kBars = 3 * PST + 2 * kNs + 2 * kNbuf + 1;
+    static constexpr int kSmem = 1024 + kData + kBars * 8 + 32;
+    static constexpr int kTmemNeed = kNbuf * BN;
+    static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
+                                   : kTmemNeed <= 256 ? 256 : 512;
     static constexpr int kHalf = BN / 2;
     static constexpr int kChunk = kHalf < 32 ? kHalf : 32;
     static_assert(kB % 1024 == 0, "stage alignment");
+    static_assert((PST * kStage) % 1024 == 0 && kSStride % 128 == 0, "TMA destination alignment");
     static_assert(kSmem <= 232448, "shared memory budget");
+    static_assert(kTmemNeed <= 512, "tensor memory budget");
 };
+
+// Barrier over `nthreads` threads (named barrier `id`) that returns whether
+// any of them passed pred = true.
+__device__ __forceinline__ bool bar_any(int id, int nthreads, bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
 
 template <int NC>
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t* r);
@@ -80,27 +115,39 @@ __global__ void __launch_bounds__(384, 1)
                     const __grid_constant__ CUtensorMap tm_s, const BlkParams p)
 {
     using Tr = BlkTraits<BN, PST>;
+    constexpr int NBUF = Tr::kNbuf;
+    constexpr int NS = Tr::kNs;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
+    uint8_t* sring = smem + PST * Tr::kStage;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Tr::kData);
-    uint64_t* full = bars;
-    uint64_t* empty = full + PST;
-    uint64_t* dfull = empty + PST;
-    uint64_t* dempty = dfull + 2;
-    uint64_t* drain = dempty + 2;
+    uint64_t* wfull = bars;             // weight tile landed
+    uint64_t* xfull = wfull + PST;      // activation tile landed
+    uint64_t* sempty = xfull + PST;     // weight + activation slot free (MMA commit)
+    uint64_t* sfull = sempty + PST;     // scales landed  [NS]
+    uint64_t* sfree = sfull + NS;       // scales consumed by the fold  [NS]
+    uint64_t* dfull = sfree + NS;       // partial product ready  [NBUF]
+    uint64_t* dempty = dfull + NBUF;    // partial buffer folded  [NBUF]
+    uint64_t* drain = dempty + NBUF;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+    int* s_last = reinterpret_cast<int*>(s_tmem + 2);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < PST; ++i) {
-            mbar_init(smem_u32(&full[i]), 1);
-            mbar_init(smem_u32(&empty[i]), 1 + 8);
+            mbar_init(smem_u32(&wfull[i]), 1);
+            mbar_init(smem_u32(&xfull[i]), 1);
+            mbar_init(smem_u32(&sempty[i]), 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(smem_u32(&sfull[i]), 1);
+            mbar_init(smem_u32(&sfree[i]), 8);
+        }
+        for (int i = 0; i < NBUF; ++i) {
             mbar_init(smem_u32(&dfull[i]), 1);
             mbar_init(smem_u32(&dempty[i]), 8);
         }
@@ -129,27 +176,55 @@ __global__ void __launch_bounds__(384, 1)
         set_error(p.err, kErrBitTimeout);
     };
 
-    if (warp == 0) {
+    if (warp == 0 || warp == 2) {
+        // ------------------------------------------------------------ producers
         if (lane == 0) {
+            const bool wprod = (warp == 0);
+            if (!wprod) {
+                // activations and their scales come from the quantization kernel
+                // launched just before; every kernel of the call triggers its
+                // dependents only after its own wait
+                grid_dep_wait();
+                grid_dep_launch();
+            }
             const uint64_t pol_w = policy_evict_first();
             const uint64_t pol_x = policy_evict_last();
-            int ps = 0;
-            uint32_t ph = 0, issued = 0, last_par = 0;
+            int ps = 0, ss = 0;
+            uint32_t ph = 0, sph = 0, issued = 0, last_par = 0, s_issued = 0, s_last_par = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 const int nb = t / per_nb, r = t % per_nb, mt = r / p.ksplit, ks = r % p.ksplit;
                 for (int kb = 0; kb < p.kb_per_split; ++kb) {
-                    if (*s_abort || !mbar_wait(smem_u32(&empty[ps]), ph ^ 1u)) {
+                    const int g = ks * p.kb_per_split + kb;
+                    if (!mbar_wait_or_abort(smem_u32(&sempty[ps]), ph ^ 1u, s_abort)) {
                         ok = false;
                         break;
                     }
-                    const int g = ks * p.kb_per_split + kb;
-                    const uint32_t fb = smem_u32(&full[ps]);
                     uint8_t* st = smem + ps * Tr::kStage;
-                    mbar_arrive_expect_tx(fb, Tr::kA + Tr::kB + BN * 4);
-                    tma_load_2d_hint(smem_u32(st), &tm_w, g * 128, nb * 128, fb, pol_w);
-                    tma_load_2d_hint(smem_u32(st + Tr::kA), &tm_x, g * 128, mt * BN, fb, pol_x);
-                    tma_load_2d(smem_u32(st + Tr::kA + Tr::kB), &tm_s, mt * BN, g, fb);
+                    if (wprod) {
+                        const uint32_t fb = smem_u32(&wfull[ps]);
+                        mbar_arrive_expect_tx(fb, Tr::kA);
+                        tma_load_2d_hint(smem_u32(st), &tm_w, g * 128, nb * 128, fb, pol_w);
+                    } else {
+                        const uint32_t fb = smem_u32(&xfull[ps]);
+                        mbar_arrive_expect_tx(fb, Tr::kB);
+                        tma_load_2d_hint(smem_u32(st + Tr::kA), &tm_x, g * 128, mt * BN, fb, pol_x);
+                        if (!mbar_wait_or_abort(smem_u32(&sfree[ss]), sph ^ 1u, s_abort)) {
+                            ok = false;
+                            issued |= 1u << ps;
+                            last_par = (last_par & ~(1u << ps)) | (ph << ps);
+                            break;
+                        }
+                        const uint32_t sb = smem_u32(&sfull[ss]);
+                        mbar_arrive_expect_tx(sb, Tr::kSBytes);
+                        tma_load_2d(smem_u32(sring + ss * Tr::kSStride), &tm_s, mt * BN, g, sb);
+                        s_issued |= 1u << ss;
+                        s_last_par = (s_last_par & ~(1u << ss)) | (sph << ss);
+                        if (++ss == NS) {
+                            ss = 0;
+                            sph ^= 1u;
+                        }
+                    }
                     issued |= 1u << ps;
                     last_par = (last_par & ~(1u << ps)) | (ph << ps);
                     if (++ps == PST) {
@@ -160,12 +235,18 @@ __global__ void __launch_bounds__(384, 1)
             }
             if (!ok) {
                 fail();
+                // let every issued copy land before the CTA's shared memory goes away
+                uint64_t* fullb = wprod ? wfull : xfull;
                 for (int s = 0; s < PST; ++s)
                     if ((issued >> s) & 1u)
-                        mbar_wait(smem_u32(&full[s]), (last_par >> s) & 1u);
+                        mbar_wait(smem_u32(&fullb[s]), (last_par >> s) & 1u);
+                for (int s = 0; s < NS; ++s)
+                    if ((s_issued >> s) & 1u)
+                        mbar_wait(smem_u32(&sfull[s]), (s_last_par >> s) & 1u);
             }
         }
     } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc = idesc_e4m3_f32(128, BN);
             int ps = 0;
@@ -173,10 +254,11 @@ __global__ void __launch_bounds__(384, 1)
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 for (int kb = 0; kb < p.kb_per_split; ++kb, ++kc) {
-                    const int d = kc & 1;
-                    const uint32_t use = kc >> 1;
-                    if (*s_abort || !mbar_wait(smem_u32(&dempty[d]), (use & 1u) ^ 1u) ||
-                        !mbar_wait(smem_u32(&full[ps]), ph)) {
+                    const int d = static_cast<int>(kc % NBUF);
+                    const uint32_t use = kc / NBUF;
+                    if (!mbar_wait_or_abort(smem_u32(&dempty[d]), (use & 1u) ^ 1u, s_abort) ||
+                        !mbar_wait_or_abort(smem_u32(&wfull[ps]), ph, s_abort) ||
+                        !mbar_wait_or_abort(smem_u32(&xfull[ps]), ph, s_abort)) {
                         ok = false;
                         break;
                     }
@@ -188,8 +270,8 @@ __global__ void __launch_bounds__(384, 1)
                     for (int kk = 0; kk < 4; ++kk)
                         umma_f8(dt, desc_kmajor_sw128(a0 + kk * 32), desc_kmajor_sw128(b0 + kk * 32),
                                 idesc, kk ? 1u : 0u);
+                    umma_commit(smem_u32(&sempty[ps]));
                     umma_commit(smem_u32(&dfull[d]));
-                    umma_commit(smem_u32(&empty[ps]));
                     if (++ps == PST) {
                         ps = 0;
                         ph ^= 1u;
@@ -203,11 +285,14 @@ __global__ void __launch_bounds__(384, 1)
             }
         }
     } else if (warp >= 4) {
+        // ------------------------------------------------------------ fold + store
+        grid_dep_wait();   // the partials and counters are this call's workspace
+        grid_dep_launch();
         const int q = warp & 3;
         const int hh = (warp - 4) >> 2;
         const int c0 = hh * Tr::kHalf;
-        int ps = 0;
-        uint32_t ph = 0, kc = 0;
+        int ss = 0;
+        uint32_t sph = 0, kc = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
             const int nb = t / per_nb, r = t % per_nb, mt = r / p.ksplit, ks = r % p.ksplit;
@@ -216,18 +301,17 @@ __global__ void __launch_bounds__(384, 1)
             for (int c = 0; c < Tr::kHalf; ++c)
                 acc[c] = 0.0f;
             for (int kb = 0; kb < p.kb_per_split; ++kb, ++kc) {
-                const int d = kc & 1;
-                const uint32_t use = kc >> 1;
-                // the stage's scales were written by TMA: observe its barrier too
-                if (*s_abort || !mbar_wait(smem_u32(&dfull[d]), use & 1u) ||
-                    !mbar_wait(smem_u32(&full[ps]), ph)) {
+                const int d = static_cast<int>(kc % NBUF);
+                const uint32_t use = kc / NBUF;
+                if (!mbar_wait_or_abort(smem_u32(&dfull[d]), use & 1u, s_abort) ||
+                    !mbar_wait_or_abort(smem_u32(&sfull[ss]), sph, s_abort)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const int g = ks * p.kb_per_split + kb;
                 const float ws = __ldg(p.wsi + static_cast<int64_t>(nb) * p.KB + g);
-                const float* xs = reinterpret_cast<const float*>(smem + ps * Tr::kStage + Tr::kA + Tr::kB);
+                const float* xs = reinterpret_cast<const float*>(sring + ss * Tr::kSStride);
                 const uint32_t tb = tmem + (static_cast<uint32_t>(q * 32) << 16) +
                                     static_cast<uint32_t>(d * BN + c0);
 #pragma unroll
@@ -245,24 +329,75 @@ __global__ void __launch_bounds__(384, 1)
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(smem_u32(&dempty[d]));
-                    mbar_arrive(smem_u32(&empty[ps]));
+                    mbar_arrive(smem_u32(&sfree[ss]));
                 }
-                if (++ps == PST) {
-                    ps = 0;
-                    ph ^= 1u;
+                if (++ss == NS) {
+                    ss = 0;
+                    sph ^= 1u;
                 }
             }
-            if (!ok)
-                break;
             const int n = nb * 128 + q * 32 + lane;
+            if (p.ksplit == 1) {
+                if (!ok)
+                    break;
 #pragma unroll
-            for (int c = 0; c < Tr::kHalf; ++c) {
-                const int m = mt * BN + c0 + c;
-                if (m < p.M) {
-                    if (p.ksplit == 1)
+                for (int c = 0; c < Tr::kHalf; ++c) {
+                    const int m = mt * BN + c0 + c;
+                    if (m < p.M)
                         p.y[static_cast<int64_t>(m) * p.N + n] = float_to_bf16_bits(acc[c]);
-                    else
+                }
+                continue;
+            }
+            if (ok) {
+#pragma unroll
+                for (int c = 0; c < Tr::kHalf; ++c) {
+                    const int m = mt * BN + c0 + c;
+                    if (m < p.M)
                         p.ypart[(static_cast<int64_t>(ks) * p.M + m) * p.N + n] = acc[c];
+                }
+            }
+            // publish the partial; the CTA that completes the tile's count sums
+            // the splits in order. Every fold warp reaches this barrier (a warp
+            // whose wait failed skipped its remaining K-blocks), and all of them
+            // leave together if any failed. The barrier orders the fold
+            // threads' stores before one thread's fence + counter increment
+            // (release); the CTA that completes the count fences (acquire)
+            // before a second barrier releases its threads to read.
+            if (bar_any(1, 256, !ok)) {
+                ok = false;
+                break;
+            }
+            if (threadIdx.x == 128) {
+                __threadfence();
+                const int old = atomicAdd(p.tile_cnt + nb * p.mt_count + mt, 1);
+                const int last = (old == p.ksplit - 1);
+                if (last)
+                    __threadfence();
+                *s_last = last;
+            }
+            asm volatile("bar.sync 1, 256;" ::: "memory");
+            if (*s_last) {
+                // the tile's outputs are spread over the 256 fold threads (n
+                // fastest: coalesced); each requests all of an output's split
+                // partials before adding them in split order
+                const int mrows = min(BN, p.M - mt * BN);
+#pragma unroll 4
+                for (int o = threadIdx.x - 128; o < 128 * mrows; o += 256) {
+                    const int m = mt * BN + o / 128;
+                    const int nn = nb * 128 + (o & 127);
+                    const float* src = p.ypart + static_cast<int64_t>(m) * p.N + nn;
+                    const int64_t step = static_cast<int64_t>(p.M) * p.N;
+                    float v[kBlkMaxKsplit];
+#pragma unroll
+                    for (int s = 0; s < kBlkMaxKsplit; ++s)
+                        if (s < p.ksplit)
+                            v[s] = __ldcg(src + s * step);
+                    float sum = 0.0f;
+#pragma unroll
+                    for (int s = 0; s < kBlkMaxKsplit; ++s)
+                        if (s < p.ksplit)
+                            sum += v[s];
+                    p.y[static_cast<int64_t>(m) * p.N + nn] = float_to_bf16_bits(sum);
                 }
             }
         }
@@ -277,27 +412,6 @@ __global__ void __launch_bounds__(384, 1)
         tc_fence_after();
         tmem_dealloc(tmem, Tr::kTmemCols);
     }
-}
-
-// y[m, n] = bf16( sum_s ypart[s, m, n] ), splits in order.
-__global__ void __launch_bounds__(256) blk_reduce_kernel(const float* __restrict__ ypart, int ksplit,
-                                                         int64_t MN, uint16_t* __restrict__ y)
-{
-    const int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 4;
-    if (i >= MN)
-        return;
-    float4 a = __ldg(reinterpret_cast<const float4*>(ypart + i));
-    for (int s = 1; s < ksplit; ++s) {
-        const float4 b = __ldg(reinterpret_cast<const float4*>(ypart + s * MN + i));
-        a.x += b.x;
-        a.y += b.y;
-        a.z += b.z;
-        a.w += b.w;
-    }
-    uint2 o;
-    o.x = float_to_bf16_bits(a.x) | (static_cast<uint32_t>(float_to_bf16_bits(a.y)) << 16);
-    o.y = float_to_bf16_bits(a.z) | (static_cast<uint32_t>(float_to_bf16_bits(a.w)) << 16);
-    *reinterpret_cast<uint2*>(y + i) = o;
 }
 
 static int blk_pick_bn(int M)
@@ -315,8 +429,8 @@ int blk_ksplit_max(int M, int K)
 {
     // split K only while the fp32 partials stay small next to the weights
     int s = K / (16 * (M < 1 ? 1 : M));
-    if (s > 16)
-        s = 16;
+    if (s > kBlkMaxKsplit)
+        s = kBlkMaxKsplit;
     if (s < 1)
         s = 1;
     return s;
@@ -328,8 +442,13 @@ BlkConfig blk_pick_config(int M, int N, int K, int num_sms)
     c.bn = blk_pick_bn(M);
     const int KB = K / 128;
     const int base = (N / 128) * ((M + c.bn - 1) / c.bn);
+    c.ksplit = 1;
+    // Splitting K costs a partial round trip and a per-tile counter hand-off
+    // on the fold path; measured on the block-FP8 shapes it pays only when
+    // the unsplit tiles leave most SMs idle (e.g. N = 2560 at M <= 8).
+    if (2 * base >= num_sms || M >= 64)
+        return c;
     const int kmax = blk_ksplit_max(M, K);
-    int best = 1;
     double best_eff = 0.0;
     for (int d = 1; d <= kmax; ++d) {
         if (KB % d != 0 || KB / d < 2)
@@ -339,10 +458,9 @@ BlkConfig blk_pick_config(int M, int N, int K, int num_sms)
         const double eff = static_cast<double>(tiles) / static_cast<double>(waves * num_sms);
         if (eff > best_eff + 0.02) {
             best_eff = eff;
-            best = d;
+            c.ksplit = d;
         }
     }
-    c.ksplit = best;
     return c;
 }
 
@@ -354,8 +472,9 @@ static int launch_blk(const CUtensorMap& tw, const CUtensorMap& tx, const CUtens
     auto kern = blk_gemm_kernel<BN, PST>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Tr::kSmem) != cudaSuccess)
         return kErrLaunch;
-    kern<<<grid, 384, Tr::kSmem, s>>>(tw, tx, ts, prm);
-    return cudaGetLastError() == cudaSuccess ? kOK : kErrLaunch;
+    return launch_dependent(kern, dim3(grid), dim3(384), Tr::kSmem, s, tw, tx, ts, prm) == cudaSuccess
+               ? kOK
+               : kErrLaunch;
 }
 
 int launch_block_gemm(const BlkLaunch& L, const BlkConfig& cfg, int num_sms, cudaStream_t s)
@@ -381,23 +500,17 @@ int launch_block_gemm(const BlkLaunch& L, const BlkConfig& cfg, int num_sms, cud
     p.nb_count = L.N / 128;
     p.wsi = L.wsi;
     p.ypart = L.ypart;
+    p.tile_cnt = L.tile_cnt;
     p.y = L.y;
     p.err = L.err;
     const int64_t tiles = static_cast<int64_t>(p.nb_count) * p.mt_count * p.ksplit;
     const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
-    int st;
     switch (BN) {
-    case 16: st = launch_blk<16, 8>(tw, tx, ts, p, grid, s); break;
-    case 32: st = launch_blk<32, 8>(tw, tx, ts, p, grid, s); break;
-    case 64: st = launch_blk<64, 8>(tw, tx, ts, p, grid, s); break;
-    default: st = launch_blk<128, 6>(tw, tx, ts, p, grid, s); break;
+    case 16: return launch_blk<16, 8>(tw, tx, ts, p, grid, s);
+    case 32: return launch_blk<32, 8>(tw, tx, ts, p, grid, s);
+    case 64: return launch_blk<64, 8>(tw, tx, ts, p, grid, s);
+    default: return launch_blk<128, 6>(tw, tx, ts, p, grid, s);
     }
-    if (st != kOK || cfg.ksplit == 1)
-        return st;
-    const int64_t MN = static_cast<int64_t>(L.M) * L.N;
-    blk_reduce_kernel<<<static_cast<unsigned>((MN / 4 + 255) / 256), 256, 0, s>>>(L.ypart, cfg.ksplit,
-                                                                                 MN, L.y);
-    return cudaGetLastError() == cudaSuccess ? kOK : kErrLaunch;
 }
 
 }  // namespace w4a8

@@ -40,7 +40,7 @@ cudaError_t launch_act_amax(const uint16_t* x, int64_t numel, float* partial, in
 cudaError_t launch_act_encode(const uint16_t* x, int64_t numel, float* scale, int compute_scale,
                               const float* partial, int nblocks, uint8_t* out, cudaStream_t s);
 cudaError_t launch_block_act_quant(const uint16_t* x, int M, int K, uint8_t* xq, float* xs_rowmajor,
-                                   float* xs_t, int ld_t, cudaStream_t s);
+                                   float* xs_t, int ld_t, int* zero, int nzero, cudaStream_t s);
 
 // ---- route.cu
 constexpr int kRouteChunk = 2048;         // assignments per histogram/scatter block
@@ -84,7 +84,7 @@ struct BlkLaunch {
     int M, N, K;
     const uint8_t* w; const float* wsi; uint16_t* y;
     const uint8_t* xq; const float* xs_t; int ld_t;
-    float* ypart; uint32_t* err;
+    float* ypart; int* tile_cnt; uint32_t* err;
 };
 int launch_block_gemm(const BlkLaunch& L, const BlkConfig& cfg, int num_sms, cudaStream_t s);
 

@@ -648,6 +648,7 @@ __global__ void __launch_bounds__(128) moe_gather_kernel(const uint8_t* __restri
 // Combine: out[t, n] = bf16( sum_j w[t,j] * a2 * S_d[e,n] * D ),
 // D = 512 * sum_splits P - s0h/64, in j then split order (deterministic).
 // ---------------------------------------------------------------------------
+template <int KS_MAX>
 __global__ void __launch_bounds__(256) moe_finalize_kernel(
     int T, int H, int k, int A, int ksplit, const int32_t* __restrict__ ids,
     const float* __restrict__ topk_w, const int32_t* __restrict__ inv,
@@ -669,18 +670,18 @@ __global__ void __launch_bounds__(256) moe_finalize_kernel(
         const int pos = __ldg(inv + a);
         const int e = __ldg(ids + a);
         const float wt = __ldg(topk_w + a);
-        // all split partials (at most kMaxKsplit) are requested before the
-        // first one is added, then summed in split order
-        float4 v[kMaxKsplit];
+        // all split partials (at most KS_MAX) are requested before the first
+        // one is added, then summed in split order
+        float4 v[KS_MAX];
 #pragma unroll
-        for (int s = 0; s < kMaxKsplit; ++s)
+        for (int s = 0; s < KS_MAX; ++s)
             if (s < ksplit)
                 v[s] = __ldg(reinterpret_cast<const float4*>(ypart + (static_cast<int64_t>(s) * A + pos) * H + n));
         const float shift = static_cast<float>(static_cast<long long>(__ldg(s0h + pos))) * (1.0f / 64.0f);
         const float4 sd = __ldg(reinterpret_cast<const float4*>(s_d + static_cast<int64_t>(e) * H + n));
         float4 P = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int s = 0; s < kMaxKsplit; ++s) {
+        for (int s = 0; s < KS_MAX; ++s) {
             if (s < ksplit) {
                 P.x += v[s].x;
                 P.y += v[s].y;
@@ -859,7 +860,10 @@ int launch_moe_forward(const MoeLaunch& L, const MoeConfig& cfg, int num_sms, cu
     mark(2);
 
     const int64_t nthreads = static_cast<int64_t>(L.T) * (L.H / 4);
-    if (launch_dependent(moe_finalize_kernel, dim3(static_cast<unsigned>((nthreads + 255) / 256)), dim3(256), 0, s,
+    // the register array of split partials is sized for the split in use
+    auto fin = cfg.ksplit == 1 ? moe_finalize_kernel<1>
+             : cfg.ksplit <= 4 ? moe_finalize_kernel<4> : moe_finalize_kernel<kMaxKsplit>;
+    if (launch_dependent(fin, dim3(static_cast<unsigned>((nthreads + 255) / 256)), dim3(256), 0, s,
                          L.T, L.H, L.k, A, cfg.ksplit, L.ids, L.topk_w, L.inv, L.ypart,
                          static_cast<const unsigned long long*>(L.s0h), L.s_d, L.a2, L.out) != cudaSuccess)
         return kErrLaunch;

@@ -203,8 +203,16 @@ cudaError_t launch_act_encode(const uint16_t* x, int64_t numel, float* scale, in
 __global__ void __launch_bounds__(256) block_act_quant_kernel(const uint16_t* __restrict__ x, int M,
                                                               int K, uint8_t* __restrict__ xq,
                                                               float* __restrict__ xs,
-                                                              float* __restrict__ xs_t, int ld_t)
+                                                              float* __restrict__ xs_t, int ld_t,
+                                                              int* __restrict__ zero, int nzero)
 {
+    // the workspace may still be in use by the previous call's GEMM
+    grid_dep_wait();
+    grid_dep_launch();
+    // clear the GEMM's split-K tile counters of this call
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nzero;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        zero[i] = 0;
     const int lane = threadIdx.x & 31;
     const int G = K / 128;
     const int64_t grp = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
@@ -230,13 +238,12 @@ __global__ void __launch_bounds__(256) block_act_quant_kernel(const uint16_t* __
 }
 
 cudaError_t launch_block_act_quant(const uint16_t* x, int M, int K, uint8_t* xq, float* xs_rowmajor,
-                                   float* xs_t, int ld_t, cudaStream_t s)
+                                   float* xs_t, int ld_t, int* zero, int nzero, cudaStream_t s)
 {
     const int64_t groups = static_cast<int64_t>(M) * (K / 128);
     const int64_t blocks = (groups + 7) / 8;
-    block_act_quant_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-        x, M, K, xq, xs_rowmajor, xs_t, ld_t);
-    return cudaGetLastError();
+    return launch_dependent(block_act_quant_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, x, M, K,
+                            xq, xs_rowmajor, xs_t, ld_t, zero, nzero);
 }
 
 }  // namespace w4a8
