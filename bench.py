@@ -401,6 +401,38 @@ def run_suite(args):
         del st
         torch.cuda.empty_cache()
 
+    # router gate fused with routing (one launch at decode) against the gate
+    # product as a separate library matmul followed by moe_route
+    for (T, H, E, k) in ((32, 4096, 8, 2), (32, 6144, 8, 2)):
+        inp = synth.router_gate_inputs(T, H, E, seed=0, device=dev)
+        ws_g = torch.zeros(lib.moe_route_gate_workspace_size(T, H, E, k), dtype=torch.uint8, device=dev)
+        ws_r = torch.zeros(lib.moe_route_workspace_size(T, E, k), dtype=torch.uint8, device=dev)
+        r_out, _ = lib.moe_route_gate(inp["hidden"], inp["gate"], k, ws=ws_g)
+        lg = torch.empty(T, E, dtype=torch.float32, device=dev)
+
+        def fused():
+            lib.moe_route_gate(inp["hidden"], inp["gate"], k, out=r_out, ws=ws_g)
+
+        def unfused():
+            torch.matmul(inp["hidden"].float(), inp["gate"].float().t(), out=lg)
+            lib.moe_route(lg, k, out=r_out, ws=ws_r)
+
+        res = {}
+        for name, fn in (("fused", fused), ("matmul_then_route", unfused)):
+            for _ in range(20):
+                fn()
+            s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            s_ev.record()
+            for _ in range(500):
+                fn()
+            e_ev.record()
+            torch.cuda.synchronize()
+            res[name] = s_ev.elapsed_time(e_ev) / 500 * 1e3
+        print(json.dumps({"suite": True, "workload": f"router gate + routing T{T} H{H} E{E} k{k}",
+                          "us_per_call": res, "launches": {"fused": 1, "matmul_then_route": "2 + casts"}}),
+              flush=True)
+
     # block-FP8 linear: four rotating weight copies (> L2) so that every call
     # reads its weights from HBM
     for (N, K) in synth.BLOCK_FP8_SHAPES:

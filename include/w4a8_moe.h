@@ -116,6 +116,33 @@ int moe_route(const float* logits, int T, int E, int k, int renormalize, int32_t
 size_t moe_route_workspace_size(int T, int E, int k);
 
 /*
+ * moe_route_gate -- the router gate and moe_route in one call: the MoE gate of
+ * PR #4152 stays unquantized (config.json ignored_layers), so its logits are
+ * computed here from the bf16 hidden states, then routed exactly as
+ * moe_route does.
+ *
+ *   hidden_bf16 [T, H] bf16 : the MoE layer's input.
+ *   gate_bf16   [E, H] bf16 : the gate weight (one row per expert).
+ *   logits_out  [T, E] fp32 : optional out (NULL allowed).
+ *                 logits[t, e] = sum_h hidden[t, h] * gate[e, h], products
+ *                 exact in fp32, accumulated in fp32 in a fixed order (the
+ *                 same inputs give the same bits).
+ *   topk_ids, topk_w, counts, offsets, sorted_ids, inv_perm: as moe_route,
+ *                 computed from those fp32 logits.
+ *   Requires T >= 1, H a positive multiple of 128, 1 <= k <= E <= 256,
+ *   T*k < 2^31. For T*k <= 4096 the whole call is one kernel.
+ *   ws: moe_route_gate_workspace_size(T, H, E, k) bytes; its first 256 bytes
+ *       must be zero before the first call on that workspace (every call
+ *       leaves them zero). Calls that share a workspace must not overlap on
+ *       the GPU.
+ */
+int moe_route_gate(const uint16_t* hidden_bf16, const uint16_t* gate_bf16, int T, int H, int E, int k,
+                   int renormalize, float* logits_out, int32_t* topk_ids, float* topk_w, int32_t* counts,
+                   int32_t* offsets, int32_t* sorted_ids, int32_t* inv_perm, void* ws, size_t ws_bytes,
+                   void* stream);
+size_t moe_route_gate_workspace_size(int T, int H, int E, int k);
+
+/*
  * moe_w4a8_forward -- the W4A8 MoE FFN (PR #7392 description: INT4 expert
  * weights upcast to FP8 so that FP8 math is used; PR #4152 Motivation: FP8
  * tensor cores, INT4 weights for lower memory bandwidth).

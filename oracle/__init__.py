@@ -58,6 +58,7 @@ def _load():
                 "orc_act_scale": (f32, [P, i64]),
                 "orc_quantize_act": (None, [P, i64, f32, P]),
                 "orc_route": (None, [P, i32, i32, i32, i32, P, P]),
+                "orc_gate_logits": (None, [P, P, i32, i32, i32, P]),
                 "orc_permute": (None, [P, i32, i32, i32, P, P, P, P]),
                 "orc_moe_forward": (None, [P, f32, i32, i32, i32, i32, i32, P, P, P, P, f32, i32,
                                            P, P, P, i32, P, i32]),
@@ -156,6 +157,17 @@ def quantize_act(x_bf16, scale: float) -> np.ndarray:
 
 
 # --- routing -----------------------------------------------------------------
+
+def gate_logits(hidden_bf16, gate_bf16) -> np.ndarray:
+    """bf16 bits hidden [T, H] and gate [E, H] -> double logits [T, E]."""
+    x = _bits16(hidden_bf16)
+    g = _bits16(gate_bf16)
+    T, H = x.shape
+    E = g.shape[0]
+    out = np.empty((T, E), np.float64)
+    _load().orc_gate_logits(_p(x), _p(g), T, H, E, _p(out))
+    return out
+
 
 def route(logits, k: int, renorm: bool = True):
     lg = _c(logits, np.float32)

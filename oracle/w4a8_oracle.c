@@ -255,6 +255,22 @@ void orc_quantize_act(const uint16_t* x, int64_t n, float scale, uint8_t* xq)
 /* Router: softmax top-k, renormalised; expert histogram; permutation        */
 /* ------------------------------------------------------------------------ */
 
+/* [P1] config.json ignored_layers: the MoE gate is not quantized, so its
+ * logits are the plain product of the bf16 hidden states and the bf16 gate
+ * weight. Computed in double (every bf16 product is exact in double):
+ *   hidden bf16 [T, H], gate bf16 [E, H] -> logits double [T, E]          */
+void orc_gate_logits(const uint16_t* hidden, const uint16_t* gate, int T, int H, int E, double* logits)
+{
+    for (int t = 0; t < T; ++t)
+        for (int e = 0; e < E; ++e) {
+            double acc = 0.0;
+            for (int h = 0; h < H; ++h)
+                acc += (double)orc_bf16_to_float(hidden[(int64_t)t * H + h]) *
+                       (double)orc_bf16_to_float(gate[(int64_t)e * H + h]);
+            logits[(int64_t)t * E + e] = acc;
+        }
+}
+
 /* [P1] num_local_experts / num_experts_per_tok and the unquantized MoE gate.
  * Readings: experts are ranked on the fp32 logits (softmax is monotone),
  * descending, equal logits ranked by lower expert index; probabilities are

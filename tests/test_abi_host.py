@@ -30,7 +30,7 @@ def test_header_lists_the_entry_points():
     names = declared_functions()
     for required in ["w4a8_quantize_experts", "w4a8_quantize_act", "moe_route", "moe_w4a8_forward",
                      "fp8_block_linear", "moe_w4a8_workspace_size", "w4a8_status_string",
-                     "w4a8_device_error"]:
+                     "w4a8_device_error", "moe_route_gate", "moe_route_gate_workspace_size"]:
         assert required in names
 
 
@@ -77,6 +77,30 @@ def test_validation_happens_before_the_device(lib):
     # everything valid, no GPU here (or a GPU that is not sm_103): device error
     if not torch.cuda.is_available():
         assert f(good, 32, 8, 2, 1, good, good, good, good, good, good, good, ws_need, None) == 5
+
+
+def test_route_gate_validation_before_the_device(lib):
+    """moe_route_gate: null, shape, alignment and workspace errors without a GPU;
+    valid arguments without an sm_103 GPU give W4A8_ERR_DEVICE."""
+    f = lib.moe_route_gate
+    P, i32 = ctypes.c_void_p, ctypes.c_int
+    f.argtypes = [P, P, i32, i32, i32, i32, i32, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
+    f.restype = i32
+    lib.moe_route_gate_workspace_size.restype = ctypes.c_size_t
+    lib.moe_route_gate_workspace_size.argtypes = [i32, i32, i32, i32]
+    good = _vp(0x10000)
+    need = lib.moe_route_gate_workspace_size(32, 4096, 8, 2)
+    assert need > 256
+
+    def call(x=good, T=32, H=4096, E=8, k=2, logits=None, ids=good, ws=good, nbytes=need):
+        return f(x, good, T, H, E, k, 1, logits, ids, good, good, good, good, good, ws, nbytes, None)
+    assert call(x=None) == 1 and call(ids=None) == 1                 # NULL
+    assert call(H=4000) == 2 and call(k=9) == 2 and call(E=300) == 2  # shape (H % 128, k > E, E > 256)
+    assert call(T=0) == 2
+    assert call(x=_vp(0x10002)) == 3 and call(logits=_vp(0x10004)) == 3   # alignment
+    assert call(nbytes=need - 1) == 4 and call(ws=None) == 4             # workspace
+    if not torch.cuda.is_available():
+        assert call() == 5                                              # no sm_103 device, no fallback
 
 
 def test_forward_shape_rules(lib):

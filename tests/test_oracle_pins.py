@@ -395,3 +395,40 @@ def test_block_quantizers_invariants():
     wq, wsi = oracle.block_quantize_weight(w)
     assert wsi.shape == (2, 1) and wsi[1, 0] == 1.0 and not wq[128:].any()
     assert (wq[:128] & 0x7F).max() == 0x7E
+
+
+# --- router gate logits ---------------------------------------------------------
+
+def test_gate_logits_match_float64_matmul():
+    """Plain double loop vs numpy's float64 matrix product of the same bf16 values."""
+    from w4a8_moe_gb300 import synth
+    inp = synth.router_gate_inputs(5, 384, 7, seed=3)
+    x = inp["hidden"].float().numpy().astype(np.float64)
+    g = inp["gate"].float().numpy().astype(np.float64)
+    got = oracle.gate_logits(inp["hidden"], inp["gate"])
+    np.testing.assert_allclose(got, x @ g.T, rtol=1e-12, atol=1e-12)
+
+
+def test_gate_logits_one_hot_rows_pick_gate_columns():
+    """Closed form: a one-hot hidden row at h (value v) gives logits v * gate[:, h] exactly."""
+    from w4a8_moe_gb300 import synth
+    g = synth.router_gate_inputs(1, 256, 9, seed=4)["gate"]
+    T, H = 6, 256
+    x = torch.zeros(T, H, dtype=torch.bfloat16)
+    cols = [0, 17, 100, 128, 200, 255]
+    vals = [1.0, -2.0, 0.5, 3.0, -0.25, 1.5]
+    for t, (h, v) in enumerate(zip(cols, vals)):
+        x[t, h] = v
+    got = oracle.gate_logits(x, g)
+    gf = g.float().numpy().astype(np.float64)
+    for t, (h, v) in enumerate(zip(cols, vals)):
+        assert np.array_equal(got[t], v * gf[:, h])
+
+
+def test_gate_logits_are_linear_in_the_gate():
+    """Doubling the gate (exact in bf16) doubles every logit exactly."""
+    from w4a8_moe_gb300 import synth
+    inp = synth.router_gate_inputs(4, 128, 5, seed=5)
+    a = oracle.gate_logits(inp["hidden"], inp["gate"])
+    b = oracle.gate_logits(inp["hidden"], (inp["gate"].float() * 2).to(torch.bfloat16))
+    assert np.array_equal(b, 2 * a)

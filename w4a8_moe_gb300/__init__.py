@@ -18,7 +18,8 @@ import torch
 __all__ = [
     "w4a8_quantize_experts", "w4a8_quantize_act", "moe_route", "moe_w4a8_forward",
     "fp8_block_linear", "w4a8_device_error", "w4a8_set_profile_events", "moe_w4a8_workspace_size",
-    "moe_route_workspace_size", "fp8_block_linear_workspace_size",
+    "moe_route_workspace_size", "fp8_block_linear_workspace_size", "moe_route_gate",
+    "moe_route_gate_workspace_size",
     "w4a8_quantize_act_workspace_size", "RouteResult", "library_path", "W4A8Error",
 ]
 
@@ -54,6 +55,8 @@ def _load():
         "w4a8_quantize_act_workspace_size": (sz, [i64]),
         "moe_route": (i32, [P, i32, i32, i32, i32, P, P, P, P, P, P, P, sz, P]),
         "moe_route_workspace_size": (sz, [i32, i32, i32]),
+        "moe_route_gate": (i32, [P, P, i32, i32, i32, i32, i32, P, P, P, P, P, P, P, P, sz, P]),
+        "moe_route_gate_workspace_size": (sz, [i32, i32, i32, i32]),
         "moe_w4a8_forward": (i32, [P, P, i32, i32, i32, i32, i32, P, P, P, P, P, i32, P, P, P, P, P,
                                    P, P, P, sz, P]),
         "moe_w4a8_workspace_size": (sz, [i32, i32, i32, i32, i32]),
@@ -103,6 +106,10 @@ def moe_w4a8_workspace_size(T, H, I, E, k) -> int:
 
 def moe_route_workspace_size(T, E, k) -> int:
     return int(_load().moe_route_workspace_size(T, E, k))
+
+
+def moe_route_gate_workspace_size(T, H, E, k) -> int:
+    return int(_load().moe_route_gate_workspace_size(T, H, E, k))
 
 
 def fp8_block_linear_workspace_size(M, N, K) -> int:
@@ -160,6 +167,29 @@ def moe_route(logits: torch.Tensor, k: int, renormalize: bool = True, out: Route
     _check(_load().moe_route(_ptr(logits), T, E, k, int(bool(renormalize)), *map(_ptr, out), _ptr(ws),
                              ws.numel(), _stream(stream)))
     return out
+
+
+def moe_route_gate(hidden: torch.Tensor, gate: torch.Tensor, k: int, renormalize: bool = True,
+                   out: RouteResult = None, logits=None, ws=None, stream=None):
+    """bf16 hidden [T, H] and bf16 router gate [E, H] -> (RouteResult, fp32 logits [T, E] or None).
+    Pass `logits` (an fp32 [T, E] tensor, or True to allocate one) to receive the logits."""
+    assert hidden.dtype == torch.bfloat16 and hidden.is_contiguous() and hidden.dim() == 2
+    assert gate.dtype == torch.bfloat16 and gate.is_contiguous() and gate.dim() == 2
+    T, H = hidden.shape
+    E = gate.shape[0]
+    dev = hidden.device
+    if out is None:
+        i32 = dict(dtype=torch.int32, device=dev)
+        out = RouteResult(torch.empty(T, k, **i32), torch.empty(T, k, dtype=torch.float32, device=dev),
+                          torch.empty(E, **i32), torch.empty(E + 1, **i32),
+                          torch.empty(T * k, **i32), torch.empty(T * k, **i32))
+    if logits is True:
+        logits = torch.empty(T, E, dtype=torch.float32, device=dev)
+    ws = _ws(moe_route_gate_workspace_size(T, H, E, k), dev, ws)
+    _check(_load().moe_route_gate(_ptr(hidden), _ptr(gate), T, H, E, k, int(bool(renormalize)),
+                                  None if logits is None else _ptr(logits), *map(_ptr, out), _ptr(ws),
+                                  ws.numel(), _stream(stream)))
+    return out, logits
 
 
 def moe_w4a8_forward(x_e4m3, a1_scale, w_gu, s_gu, w_d, s_d, a2_scale, act: int,

@@ -101,6 +101,30 @@ bool encode_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base
 }
 
 // ---- workspace layouts ------------------------------------------------------
+// Router with the gate: the header holds the grid-wide completion counter of
+// the one-launch path (byte 128); then logits (when the caller wants none),
+// the per-slice partial logits and the multi-kernel path's histograms.
+struct RouteGateWs {
+    int* done;
+    float* logits;
+    float* partial;
+    int32_t* hist;
+    int32_t* base;
+};
+static size_t route_gate_ws(int T, int H, int E, int k, RouteGateWs* w, void* ws)
+{
+    Carver c(ws);
+    w->done = ws ? reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + 128) : nullptr;
+    w->logits = c.take<float>(static_cast<size_t>(T) * E * 4);
+    const int hs = route_gate_slice(T, H, E, k);
+    w->partial = c.take<float>(hs ? static_cast<size_t>(H / hs) * T * E * 4 : 0);
+    const int64_t A = static_cast<int64_t>(T) * k;
+    const int64_t nb = (A + kRouteChunk - 1) / kRouteChunk;
+    w->hist = c.take<int32_t>(static_cast<size_t>(nb) * E * 4);
+    w->base = c.take<int32_t>(static_cast<size_t>(nb) * E * 4);
+    return c.off;
+}
+
 static size_t route_ws(int T, int E, int k, int32_t** hist, int32_t** base, void* ws)
 {
     Carver c(ws);
@@ -229,6 +253,45 @@ size_t moe_route_workspace_size(int T, int E, int k)
 {
     int32_t *h, *b;
     return route_ws(T, E, k, &h, &b, nullptr);
+}
+
+size_t moe_route_gate_workspace_size(int T, int H, int E, int k)
+{
+    RouteGateWs w;
+    return route_gate_ws(T, H, E, k, &w, nullptr);
+}
+
+int moe_route_gate(const uint16_t* hidden_bf16, const uint16_t* gate_bf16, int T, int H, int E, int k,
+                   int renormalize, float* logits_out, int32_t* topk_ids, float* topk_w, int32_t* counts,
+                   int32_t* offsets, int32_t* sorted_ids, int32_t* inv_perm, void* ws, size_t ws_bytes,
+                   void* stream)
+{
+    if (!hidden_bf16 || !gate_bf16 || !topk_ids || !topk_w || !counts || !offsets || !sorted_ids || !inv_perm)
+        return W4A8_ERR_NULL;
+    if (T < 1 || H < 128 || H % 128 != 0 || E < 1 || E > 256 || k < 1 || k > E ||
+        static_cast<int64_t>(T) * k >= (static_cast<int64_t>(1) << 31))
+        return W4A8_ERR_SHAPE;
+    const void* ptrs[] = {hidden_bf16, gate_bf16, topk_ids, topk_w, counts, offsets, sorted_ids, inv_perm};
+    for (const void* p : ptrs)
+        if (!aligned16(p))
+            return W4A8_ERR_ALIGN;
+    if (logits_out && !aligned16(logits_out))
+        return W4A8_ERR_ALIGN;
+    if (!ws || ws_bytes < moe_route_gate_workspace_size(T, H, E, k))
+        return W4A8_ERR_WORKSPACE;
+    if (!aligned16(ws))
+        return W4A8_ERR_ALIGN;
+    int sms;
+    if (int st = current_device(&sms))
+        return st;
+    RouteGateWs w;
+    route_gate_ws(T, H, E, k, &w, ws);
+    float* logits = logits_out ? logits_out : w.logits;
+    return launch_route_gate(hidden_bf16, gate_bf16, T, H, E, k, renormalize ? 1 : 0, logits, topk_ids, topk_w,
+                             counts, offsets, sorted_ids, inv_perm, w.partial, w.done, w.hist, w.base,
+                             static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? W4A8_OK
+               : W4A8_ERR_LAUNCH;
 }
 
 int moe_route(const float* logits, int T, int E, int k, int renormalize, int32_t* topk_ids,

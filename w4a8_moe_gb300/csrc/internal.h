@@ -45,9 +45,15 @@ cudaError_t launch_block_act_quant(const uint16_t* x, int M, int K, uint8_t* xq,
 // ---- route.cu
 constexpr int kRouteChunk = 2048;         // assignments per histogram/scatter block
 constexpr int kRouteFusedMax = 4096;      // T*k up to which one block does everything
+constexpr int kRouteGatePartials = 16384; // fp32 partial logits the one-launch gate path reduces
 cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, int32_t* ids,
                          float* w, int32_t* counts, int32_t* offsets, int32_t* sorted_ids,
                          int32_t* inv, int32_t* block_hist, int32_t* block_base, cudaStream_t s);
+int route_gate_slice(int T, int H, int E, int k);
+cudaError_t launch_route_gate(const uint16_t* x, const uint16_t* gate, int T, int H, int E, int k,
+                              int renorm, float* logits, int32_t* ids, float* w, int32_t* counts,
+                              int32_t* offsets, int32_t* sorted_ids, int32_t* inv, float* partial,
+                              int* done, int32_t* block_hist, int32_t* block_base, cudaStream_t s);
 
 // ---- moe.cu
 constexpr int kMaxKsplit = 16;   // largest split of the down projection's K

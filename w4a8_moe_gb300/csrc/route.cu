@@ -18,7 +18,16 @@ namespace w4a8 {
 
 constexpr int kMaxE = 256;
 
+// Logits are read through the read-only path when they come from an earlier
+// kernel, with plain loads when the same kernel has just written them.
+template <bool kPlain>
+__device__ __forceinline__ float load_logit(const float* p)
+{
+    return kPlain ? *p : __ldg(p);
+}
+
 // One warp per token; lane l holds logits l, l+32, ... (E <= 256).
+template <bool kPlain = false>
 __device__ __forceinline__ void route_token(const float* __restrict__ logits, int t, int E, int k,
                                             int renorm, int32_t* __restrict__ ids,
                                             float* __restrict__ w, int32_t* s_ids)
@@ -28,7 +37,7 @@ __device__ __forceinline__ void route_token(const float* __restrict__ logits, in
 #pragma unroll
     for (int i = 0; i < kMaxE / 32; ++i) {
         const int e = lane + 32 * i;
-        v[i] = (e < E) ? __ldg(logits + static_cast<int64_t>(t) * E + e) : -INFINITY;
+        v[i] = (e < E) ? load_logit<kPlain>(logits + static_cast<int64_t>(t) * E + e) : -INFINITY;
     }
     uint32_t taken = 0;  // bit i: entry lane + 32 i already selected
     float mx = -INFINITY;
@@ -87,7 +96,7 @@ __device__ __forceinline__ void route_token(const float* __restrict__ logits, in
             if (j < 8) {
                 lv = sel_val[j];
             } else {
-                lv = __ldg(logits + static_cast<int64_t>(t) * E + ids[static_cast<int64_t>(t) * k + j]);
+                lv = load_logit<kPlain>(logits + static_cast<int64_t>(t) * E + ids[static_cast<int64_t>(t) * k + j]);
             }
             w[static_cast<int64_t>(t) * k + j] = __fdiv_rn(expf(lv - mx), denom);
         }
@@ -231,27 +240,18 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(const int32_t* __res
 
 // Small problems (T*k <= kRouteFusedMax): one block of 512 threads does
 // top-k, histogram, scan and scatter.
-__global__ void __launch_bounds__(512) route_fused_kernel(const float* __restrict__ logits, int T,
-                                                           int E, int k, int renorm,
-                                                           int32_t* __restrict__ ids,
-                                                           float* __restrict__ w,
-                                                           int32_t* __restrict__ counts,
-                                                           int32_t* __restrict__ offsets,
-                                                           int32_t* __restrict__ sorted_ids,
-                                                           int32_t* __restrict__ inv)
+// Histogram, scan and stable scatter of A <= kRouteFusedMax assignments whose
+// experts are in s_ids (shared memory), by one block of 512 threads. Starts
+// with a block barrier (s_ids written by other warps).
+__device__ __forceinline__ void route_block_tail(const int32_t* s_ids, int A, int E,
+                                                 int32_t* __restrict__ counts,
+                                                 int32_t* __restrict__ offsets,
+                                                 int32_t* __restrict__ sorted_ids,
+                                                 int32_t* __restrict__ inv, int* cnt, int* base,
+                                                 int (*wcnt)[kMaxE])
 {
-    grid_dep_wait();
-    grid_dep_launch();
-    __shared__ int32_t s_ids[kRouteFusedMax];
-    __shared__ int cnt[kMaxE];
-    __shared__ int base[kMaxE];
-    __shared__ int wcnt[16][kMaxE];
-    const int A = T * k;
-    const int wid = threadIdx.x >> 5;
     for (int e = threadIdx.x; e < E; e += blockDim.x)
         cnt[e] = 0;
-    for (int t = wid; t < T; t += 16)
-        route_token(logits, t, E, k, renorm, ids, w, s_ids);
     __syncthreads();
     for (int a = threadIdx.x; a < A; a += blockDim.x)
         atomicAdd(&cnt[s_ids[a]], 1);
@@ -273,6 +273,181 @@ __global__ void __launch_bounds__(512) route_fused_kernel(const float* __restric
     scatter_chunk<16>(s_ids, 0, A, E, base, cnt, wcnt, sorted_ids, inv);
 }
 
+__global__ void __launch_bounds__(512) route_fused_kernel(const float* __restrict__ logits, int T,
+                                                           int E, int k, int renorm,
+                                                           int32_t* __restrict__ ids,
+                                                           float* __restrict__ w,
+                                                           int32_t* __restrict__ counts,
+                                                           int32_t* __restrict__ offsets,
+                                                           int32_t* __restrict__ sorted_ids,
+                                                           int32_t* __restrict__ inv)
+{
+    grid_dep_wait();
+    grid_dep_launch();
+    __shared__ int32_t s_ids[kRouteFusedMax];
+    __shared__ int cnt[kMaxE];
+    __shared__ int base[kMaxE];
+    __shared__ int wcnt[16][kMaxE];
+    const int A = T * k;
+    const int wid = threadIdx.x >> 5;
+    for (int t = wid; t < T; t += 16)
+        route_token(logits, t, E, k, renorm, ids, w, s_ids);
+    route_block_tail(s_ids, A, E, counts, offsets, sorted_ids, inv, cnt, base, wcnt);
+}
+
+// ---------------------------------------------------------------------------
+// Router gate fused with routing: logits[t, e] = sum_h x[t, h] * G[e, h] in
+// fp32 (bf16 operands, exact products), then the same top-k, histogram and
+// permutation as above.
+//
+// "ROCm: enable trillion-parameter MoE models with INT4-FP8 single node",
+// config.json: ignored_layers keeps the MoE gate unquantized, so it runs on the
+// bf16 hidden states.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// Small problems, one launch: block s computes the partial logits of H slice
+// [s*HS, (s+1)*HS) for every token (one warp per token, 8 elements per lane for
+// HS = 256, a fixed butterfly per expert) into partial[s, t, e]; the block that
+// completes the grid-wide count sums the slices in order, routes every token
+// and builds the permutation. `done` is zero at entry and left zero.
+__global__ void __launch_bounds__(512) route_gate_fused_kernel(
+    const uint16_t* __restrict__ x, const uint16_t* __restrict__ gate, int T, int H, int E, int k,
+    int renorm, int HS, float* __restrict__ partial, float* __restrict__ logits, int32_t* __restrict__ ids,
+    float* __restrict__ w, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ sorted_ids, int32_t* __restrict__ inv, int* __restrict__ done)
+{
+    grid_dep_wait();
+    grid_dep_launch();
+    extern __shared__ __align__(16) uint8_t dyn[];
+    __shared__ int32_t s_ids[kRouteFusedMax];
+    __shared__ int cnt[kMaxE];
+    __shared__ int base[kMaxE];
+    __shared__ int wcnt[16][kMaxE];
+    __shared__ int s_last;
+    const int S = gridDim.x;
+    const int s = blockIdx.x;
+    const int h0 = s * HS;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int per_lane = HS / 32;   // 4, 8 or 16 elements, consecutive
+    // the gate slice [E, HS] in shared memory (bf16)
+    uint16_t* g_s = reinterpret_cast<uint16_t*>(dyn);
+    const int chunks = E * (HS / 8);
+    for (int i = threadIdx.x; i < chunks; i += blockDim.x) {
+        const int e = i / (HS / 8), c = i % (HS / 8);
+        reinterpret_cast<uint4*>(g_s)[i] =
+            __ldg(reinterpret_cast<const uint4*>(gate + static_cast<int64_t>(e) * H + h0) + c);
+    }
+    __syncthreads();
+    for (int t = wid; t < T; t += 16) {
+        float xv[16];
+        const uint16_t* xr = x + static_cast<int64_t>(t) * H + h0 + lane * per_lane;
+#pragma unroll
+        for (int q = 0; q < 16; q += 8) {
+            if (q + 8 <= per_lane) {   // 16-byte loads only for 8 or 16 elements per lane
+                const uint4 u = __ldg(reinterpret_cast<const uint4*>(xr + q));
+                xv[q + 0] = bf16_lo(u.x); xv[q + 1] = bf16_hi(u.x);
+                xv[q + 2] = bf16_lo(u.y); xv[q + 3] = bf16_hi(u.y);
+                xv[q + 4] = bf16_lo(u.z); xv[q + 5] = bf16_hi(u.z);
+                xv[q + 6] = bf16_lo(u.w); xv[q + 7] = bf16_hi(u.w);
+            }
+        }
+        if (per_lane == 4) {
+            const uint2 u = __ldg(reinterpret_cast<const uint2*>(xr));
+            xv[0] = bf16_lo(u.x); xv[1] = bf16_hi(u.x); xv[2] = bf16_lo(u.y); xv[3] = bf16_hi(u.y);
+        }
+        for (int e = 0; e < E; ++e) {
+            const uint16_t* gr = g_s + e * HS + lane * per_lane;
+            float acc = 0.0f;
+#pragma unroll
+            for (int q = 0; q < 16; q += 2) {
+                if (q < per_lane) {
+                    const uint32_t gp = *reinterpret_cast<const uint32_t*>(gr + q);
+                    acc = fmaf(xv[q], bf16_lo(gp), acc);
+                    acc = fmaf(xv[q + 1], bf16_hi(gp), acc);
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+            if (lane == 0)
+                partial[(static_cast<int64_t>(s) * T + t) * E + e] = acc;
+        }
+    }
+    // the last block to finish routes
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const int old = atomicAdd(done, 1);
+        const int last = (old == S - 1);
+        if (last)
+            __threadfence();
+        s_last = last;
+    }
+    __syncthreads();
+    if (!s_last)
+        return;
+    const int TE = T * E;
+    float* red = reinterpret_cast<float*>(dyn);   // S*T*E partials (the gate slice is no longer needed)
+#pragma unroll 8
+    for (int i = threadIdx.x; i < S * TE; i += blockDim.x)
+        red[i] = __ldcg(partial + i);
+    __syncthreads();
+    for (int i = threadIdx.x; i < TE; i += blockDim.x) {
+        float acc = 0.0f;
+        for (int q = 0; q < S; ++q)
+            acc += red[q * TE + i];
+        logits[i] = acc;
+    }
+    __syncthreads();
+    for (int t = wid; t < T; t += 16)
+        route_token<true>(logits, t, E, k, renorm, ids, w, s_ids);
+    route_block_tail(s_ids, T * k, E, counts, offsets, sorted_ids, inv, cnt, base, wcnt);
+    if (threadIdx.x == 0)
+        *done = 0;
+}
+
+// Larger problems: one warp per token computes its E logits over the whole H
+// (gate rows read through L2), writes them and routes the token.
+__global__ void __launch_bounds__(256) route_gate_topk_kernel(const uint16_t* __restrict__ x,
+                                                              const uint16_t* __restrict__ gate, int T,
+                                                              int H, int E, int k, int renorm,
+                                                              float* __restrict__ logits,
+                                                              int32_t* __restrict__ ids,
+                                                              float* __restrict__ w)
+{
+    grid_dep_wait();
+    grid_dep_launch();
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (t >= T)
+        return;
+    const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t) * H);
+    for (int e = 0; e < E; ++e) {
+        const uint4* gr = reinterpret_cast<const uint4*>(gate + static_cast<int64_t>(e) * H);
+        float acc = 0.0f;
+        for (int c = lane; c < H / 8; c += 32) {
+            const uint4 a = __ldg(xr + c), b = __ldg(gr + c);
+            acc = fmaf(bf16_lo(a.x), bf16_lo(b.x), acc);
+            acc = fmaf(bf16_hi(a.x), bf16_hi(b.x), acc);
+            acc = fmaf(bf16_lo(a.y), bf16_lo(b.y), acc);
+            acc = fmaf(bf16_hi(a.y), bf16_hi(b.y), acc);
+            acc = fmaf(bf16_lo(a.z), bf16_lo(b.z), acc);
+            acc = fmaf(bf16_hi(a.z), bf16_hi(b.z), acc);
+            acc = fmaf(bf16_lo(a.w), bf16_lo(b.w), acc);
+            acc = fmaf(bf16_hi(a.w), bf16_hi(b.w), acc);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+        if (lane == 0)
+            logits[static_cast<int64_t>(t) * E + e] = acc;
+    }
+    __syncwarp();
+    route_token<true>(logits, t, E, k, renorm, ids, w, nullptr);
+}
+
 cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, int32_t* ids,
                          float* w, int32_t* counts, int32_t* offsets, int32_t* sorted_ids,
                          int32_t* inv, int32_t* block_hist, int32_t* block_base, cudaStream_t s)
@@ -284,6 +459,54 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, i
     const int nb = (A + kRouteChunk - 1) / kRouteChunk;
     cudaError_t e = launch_dependent(route_topk_kernel, dim3((T + 7) / 8), dim3(256), 0, s, logits, T, E, k,
                                      renorm, ids, w);
+    if (e == cudaSuccess)
+        e = launch_dependent(route_hist_kernel, dim3(nb), dim3(256), 0, s,
+                             static_cast<const int32_t*>(ids), A, E, block_hist);
+    if (e == cudaSuccess)
+        e = launch_dependent(route_scan_kernel, dim3(1), dim3(256), 0, s, static_cast<const int32_t*>(block_hist),
+                             nb, E, A, counts, offsets, block_base);
+    if (e == cudaSuccess)
+        e = launch_dependent(route_scatter_kernel, dim3(nb), dim3(256), 0, s, static_cast<const int32_t*>(ids), A,
+                             E, static_cast<const int32_t*>(block_base), sorted_ids, inv);
+    return e;
+}
+
+// Slice width of the one-launch gate path: the smallest of 128/256/512 whose
+// S x T x E partials fit the reduction buffer, or 0 when none does (or when
+// the problem is too large for one block to route).
+int route_gate_slice(int T, int H, int E, int k)
+{
+    if (static_cast<int64_t>(T) * k > kRouteFusedMax)
+        return 0;
+    for (int hs = 128; hs <= 512; hs *= 2) {
+        if (H % hs != 0)
+            continue;
+        const int64_t s = H / hs;
+        if (s * T * E <= kRouteGatePartials && static_cast<int64_t>(E) * hs * 2 <= kRouteGatePartials * 4)
+            return hs;
+    }
+    return 0;
+}
+
+cudaError_t launch_route_gate(const uint16_t* x, const uint16_t* gate, int T, int H, int E, int k,
+                              int renorm, float* logits, int32_t* ids, float* w, int32_t* counts,
+                              int32_t* offsets, int32_t* sorted_ids, int32_t* inv, float* partial,
+                              int* done, int32_t* block_hist, int32_t* block_base, cudaStream_t s)
+{
+    const int A = T * k;
+    const int hs = route_gate_slice(T, H, E, k);
+    if (hs) {
+        const size_t dyn = static_cast<size_t>(kRouteGatePartials) * 4;
+        cudaError_t e = cudaFuncSetAttribute(route_gate_fused_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(dyn));
+        if (e != cudaSuccess)
+            return e;
+        return launch_dependent(route_gate_fused_kernel, dim3(H / hs), dim3(512), dyn, s, x, gate, T, H, E, k,
+                                renorm, hs, partial, logits, ids, w, counts, offsets, sorted_ids, inv, done);
+    }
+    const int nb = (A + kRouteChunk - 1) / kRouteChunk;
+    cudaError_t e = launch_dependent(route_gate_topk_kernel, dim3((T + 7) / 8), dim3(256), 0, s, x, gate, T, H,
+                                     E, k, renorm, logits, ids, w);
     if (e == cudaSuccess)
         e = launch_dependent(route_hist_kernel, dim3(nb), dim3(256), 0, s,
                              static_cast<const int32_t*>(ids), A, E, block_hist);

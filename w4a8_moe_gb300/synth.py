@@ -97,6 +97,13 @@ def block_fp8_inputs(M: int, N: int, K: int, seed: int = 0, device="cpu", weight
     return {"x": x.contiguous(), "w": w.contiguous()}
 
 
+def router_gate_inputs(T: int, H: int, E: int, seed: int = 0, device="cpu", gate_std: float = 0.02):
+    """Hidden states bf16 [T, H] ~ N(0, 1) and a router gate bf16 [E, H] ~ N(0, gate_std)."""
+    x = torch.randn(T, H, generator=_gen(seed, device, 8), device=device).to(torch.bfloat16)
+    g = (torch.randn(E, H, generator=_gen(seed, device, 9), device=device) * gate_std).to(torch.bfloat16)
+    return {"hidden": x.contiguous(), "gate": g.contiguous()}
+
+
 def calibration_tokens(T: int, n: int = 8):
     """Tokens the static intermediate scale is calibrated on: the first min(T, n)."""
     return list(range(min(T, n)))
