@@ -67,6 +67,7 @@ def _load():
                 "orc_block_quantize_weight": (None, [P, i32, i32, P, P]),
                 "orc_block_quantize_act": (None, [P, i32, i32, P, P]),
                 "orc_block_linear": (None, [P, P, i32, i32, i32, P, P, P, i32, P, i32]),
+                "orc_fp8_linear": (None, [P, f32, i32, i32, i32, P, f32, P, i32, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -258,4 +259,16 @@ def block_linear(xq, xs, wq, wsi, rows=None, nthreads=1) -> np.ndarray:
     y = np.empty((r.size, N), np.float64)
     _load().orc_block_linear(_p(xq), _p(xs), M, N, K, _p(wq), _p(wsi), _p(r), r.size, _p(y),
                              int(nthreads))
+    return y
+
+
+def fp8_linear(xq, sx: float, wq, sw: float, rows=None) -> np.ndarray:
+    """Per-tensor FP8 linear: codes xq [M, K], wq [N, K] with scales sx, sw -> double y [rows, N]."""
+    xq = _c(xq, np.uint8)
+    wq = _c(wq, np.uint8)
+    M, K = xq.shape
+    N = wq.shape[0]
+    r = _c(np.arange(M) if rows is None else rows, np.int32)
+    y = np.empty((r.size, N), np.float64)
+    _load().orc_fp8_linear(_p(xq), float(sx), M, N, K, _p(wq), float(sw), _p(r), r.size, _p(y))
     return y

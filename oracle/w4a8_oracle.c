@@ -633,3 +633,37 @@ void orc_block_linear(const uint8_t* xq, const float* xs, int M, int N, int K, c
     free(th);
     free(jobs);
 }
+
+/* ------------------------------------------------------------------------ */
+/* Per-tensor FP8 dense linear                                               */
+/* ------------------------------------------------------------------------ */
+
+/* [P2] description: the attention projections are quantized online to float8;
+ * review summary: QuarkInt4Fp8LinearMethod for linear layers and tensor-wise
+ * FP8 quantization. Reading: one scale for the whole weight (sw) and one for
+ * the activations (sx), both from the tensor-wise quantizer, so
+ *   y[m, n] = sx * sw * sum_k dec(xq[m, k]) * dec(wq[n, k])
+ * with the inner sum exact (int64 on 512*dec values; products are multiples
+ * of 2^-18).   xq u8 [M, K], wq u8 [N, K] -> y double [rows, N]           */
+void orc_fp8_linear(const uint8_t* xq, float sx, int M, int N, int K, const uint8_t* wq, float sw,
+                    const int32_t* rows, int nrows, double* y)
+{
+    int64_t* w512 = (int64_t*)malloc(sizeof(int64_t) * (size_t)K);
+    int64_t* x512 = (int64_t*)malloc(sizeof(int64_t) * (size_t)K);
+    (void)M;
+    for (int ri = 0; ri < nrows; ++ri) {
+        int m = rows[ri];
+        for (int k = 0; k < K; ++k)
+            x512[k] = orc_e4m3_times512(xq[(int64_t)m * K + k]);
+        for (int n = 0; n < N; ++n) {
+            int64_t acc = 0;
+            for (int k = 0; k < K; ++k)
+                w512[k] = orc_e4m3_times512(wq[(int64_t)n * K + k]);
+            for (int k = 0; k < K; ++k)
+                acc += x512[k] * w512[k];
+            y[(int64_t)ri * N + n] = (double)sx * (double)sw * ((double)acc / 262144.0);
+        }
+    }
+    free(w512);
+    free(x512);
+}

@@ -432,3 +432,46 @@ def test_gate_logits_are_linear_in_the_gate():
     a = oracle.gate_logits(inp["hidden"], inp["gate"])
     b = oracle.gate_logits(inp["hidden"], (inp["gate"].float() * 2).to(torch.bfloat16))
     assert np.array_equal(b, 2 * a)
+
+
+# --- per-tensor FP8 linear ------------------------------------------------------
+
+def _fp8_codes(shape, rng):
+    """Random finite E4M3 codes (NaN codes 0x7F/0xFF excluded)."""
+    c = rng.integers(0, 256, size=shape, dtype=np.uint8)
+    return np.where((c & 0x7F) == 0x7F, c ^ 0x01, c).astype(np.uint8)
+
+
+def test_fp8_linear_equals_block_linear_with_uniform_scales():
+    """With every block scale equal to sw and every activation group scale sx,
+    the block-FP8 definition (pinned separately) is the per-tensor one."""
+    rng = np.random.default_rng(21)
+    M, N, K = 5, 256, 384
+    xq, wq = _fp8_codes((M, K), rng), _fp8_codes((N, K), rng)
+    sx, sw = np.float32(0.013), np.float32(0.0021)
+    y = oracle.fp8_linear(xq, sx, wq, sw)
+    xs = np.full((M, K // 128), sx, np.float32)
+    wsi = np.full((N // 128, K // 128), sw, np.float32)
+    yb = oracle.block_linear(xq, xs, wq, wsi)
+    np.testing.assert_allclose(y, yb, rtol=1e-13, atol=0)
+
+
+def test_fp8_linear_integer_codes_unit_scales_is_an_integer_gemm():
+    """E4M3 codes of small integers with unit scales: an exact int64 matrix product."""
+    rng = np.random.default_rng(22)
+    M, N, K = 4, 128, 256
+    table = {v: int(oracle.e4m3_from_float(np.float32(v))[0]) for v in range(-8, 9)}
+    xi = rng.integers(-8, 9, size=(M, K))
+    wi = rng.integers(-8, 9, size=(N, K))
+    xq = np.vectorize(table.get)(xi).astype(np.uint8)
+    wq = np.vectorize(table.get)(wi).astype(np.uint8)
+    y = oracle.fp8_linear(xq, 1.0, wq, 1.0)
+    assert np.array_equal(y, (xi.astype(np.int64) @ wi.astype(np.int64).T).astype(np.float64))
+
+
+def test_fp8_linear_scales_by_powers_of_two_exactly():
+    rng = np.random.default_rng(23)
+    xq, wq = _fp8_codes((3, 256), rng), _fp8_codes((128, 256), rng)
+    a = oracle.fp8_linear(xq, 0.5, wq, 0.25)
+    b = oracle.fp8_linear(xq, 0.5 * 2 ** 5, wq, 0.25 * 2 ** -3)
+    assert np.array_equal(b, a * 4)

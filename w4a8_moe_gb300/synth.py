@@ -104,6 +104,19 @@ def router_gate_inputs(T: int, H: int, E: int, seed: int = 0, device="cpu", gate
     return {"hidden": x.contiguous(), "gate": g.contiguous()}
 
 
+# Per-tensor FP8 dense projections of a Grok-1-shaped attention block
+# (hidden 6144, 48 query heads and 8 key/value heads of 128): qkv_proj and o_proj.
+FP8_LINEAR_SHAPES = [(8192, 6144), (6144, 6144)]
+FP8_LINEAR_M = [1, 8, 64, 4096]
+
+
+def fp8_linear_inputs(M: int, N: int, K: int, seed: int = 0, device="cpu", weight_std: float = 0.02):
+    """Activations x bf16 [M, K] ~ N(0, 1) and a dense weight bf16 [N, K] ~ N(0, weight_std)."""
+    x = torch.randn(M, K, generator=_gen(seed, device, 10), device=device).to(torch.bfloat16)
+    w = (torch.randn(N, K, generator=_gen(seed, device, 11), device=device) * weight_std).to(torch.bfloat16)
+    return {"x": x.contiguous(), "w": w.contiguous()}
+
+
 def calibration_tokens(T: int, n: int = 8):
     """Tokens the static intermediate scale is calibrated on: the first min(T, n)."""
     return list(range(min(T, n)))
