@@ -433,6 +433,48 @@ def run_suite(args):
                           "us_per_call": res, "launches": {"fused": 1, "matmul_then_route": "2 + casts"}}),
               flush=True)
 
+    # per-tensor FP8 linear (Grok-1 attention projections), four rotating
+    # weight copies (> L2)
+    for (N, K) in synth.FP8_LINEAR_SHAPES:
+        wl, swl = [], []
+        for c in range(4):
+            w = synth.fp8_linear_inputs(1, N, K, seed=c, device=dev)["w"]
+            q, s_ = lib.w4a8_quantize_act(w)
+            wl.append(q)
+            swl.append(s_)
+            del w
+        for M in synth.FP8_LINEAR_M:
+            x = synth.fp8_linear_inputs(M, N, K, seed=9, device=dev)["x"]
+            xq, sx = lib.w4a8_quantize_act(x)
+            y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+            wsp = torch.zeros(lib.fp8_linear_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
+            iters = 400 if M <= 64 else 40
+            for i in range(8):
+                lib.fp8_linear(xq, sx, wl[i % 4], swl[i % 4], out=y, ws=wsp)
+            torch.cuda.synchronize()
+            s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s_ev.record()
+            for i in range(iters):
+                lib.fp8_linear(xq, sx, wl[i % 4], swl[i % 4], out=y, ws=wsp)
+            e_ev.record()
+            torch.cuda.synchronize()
+            assert lib.w4a8_device_error(wsp) == 0, "device error word set"
+            ms = s_ev.elapsed_time(e_ev) / iters
+            nbytes = N * K + M * K + 2 * M * N
+            flops = 2.0 * M * N * K
+            line = {"suite": True, "workload": f"per-tensor FP8 linear N{N} K{K} M{M}", "ms_per_call": ms,
+                    "gbs": nbytes / (ms * 1e-3) / 1e9, "tflops": flops / (ms * 1e-3) / 1e12,
+                    "l2": "4 rotating weight copies"}
+            if M <= 64:
+                line.update({"bound": "hbm", "frac": line["gbs"] / hbm, "peak_gbs": hbm,
+                             "peak_source": src + " hbm_gbs"})
+            else:
+                line.update({"bound": "tensor", "frac": line["tflops"] / fp8_burst, "peak_tflops": fp8_burst,
+                             "peak_source": src + " bf16_tflops x 2 (nominal fp8/bf16)"})
+            print(json.dumps(line), flush=True)
+        del wl, swl
+        torch.cuda.empty_cache()
+
     # block-FP8 linear: four rotating weight copies (> L2) so that every call
     # reads its weights from HBM
     for (N, K) in synth.BLOCK_FP8_SHAPES:

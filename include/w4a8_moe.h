@@ -211,6 +211,29 @@ int moe_w4a8_forward_static(const uint8_t* x_e4m3, const float* a1_scale, int T,
                             const int32_t* inv_perm, uint16_t* out_bf16, void* stream);
 
 /*
+ * fp8_linear -- per-tensor FP8 dense projection ("[AMD][Quantization] Add
+ * int4fp8_moe online quantization on ROCm", description: the attention
+ * projections are quantized online to float8; review summary:
+ * QuarkInt4Fp8LinearMethod, tensor-wise FP8 quantization).
+ *
+ *   y[m, n] = bf16( x_scale * w_scale * sum_k dec(x_e4m3[m, k]) * dec(w_e4m3[n, k]) )
+ * with fp32 tensor-core accumulation.
+ *
+ *   x_e4m3 [M, K] u8, x_scale [1] fp32 (device): e.g. from w4a8_quantize_act.
+ *   w_e4m3 [N, K] u8, w_scale [1] fp32 (device): the weight quantized with
+ *          w4a8_quantize_act (compute_scale = 1) once, at load.
+ *   y_bf16 [M, N]: out.
+ *   Requires M >= 1, N and K positive multiples of 128.
+ *   ws: fp8_linear_workspace_size(M, N, K) bytes, zero-filled before its first
+ *       use with this function (calls leave the split-K counters at zero; after
+ *       a W4A8_ERR_TIMEOUT report, zero it again). Calls that share a workspace
+ *       must not overlap on the GPU.
+ */
+int fp8_linear(const uint8_t* x_e4m3, const float* x_scale, int M, int N, int K, const uint8_t* w_e4m3,
+               const float* w_scale, uint16_t* y_bf16, void* ws, size_t ws_bytes, void* stream);
+size_t fp8_linear_workspace_size(int M, int N, int K);
+
+/*
  * fp8_block_linear -- block-FP8 dense projection y = x W^T (PR #392
  * description: FP8_PB_WO weights consumed with their weight_scale_inv, one
  * fp32 scale per 128-row x 128-col block).

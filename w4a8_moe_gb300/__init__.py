@@ -19,7 +19,7 @@ __all__ = [
     "w4a8_quantize_experts", "w4a8_quantize_act", "moe_route", "moe_w4a8_forward",
     "fp8_block_linear", "w4a8_device_error", "w4a8_set_profile_events", "moe_w4a8_workspace_size",
     "moe_route_workspace_size", "fp8_block_linear_workspace_size", "moe_route_gate",
-    "moe_route_gate_workspace_size",
+    "moe_route_gate_workspace_size", "fp8_linear", "fp8_linear_workspace_size",
     "w4a8_quantize_act_workspace_size", "RouteResult", "library_path", "W4A8Error",
 ]
 
@@ -62,6 +62,8 @@ def _load():
         "moe_w4a8_workspace_size": (sz, [i32, i32, i32, i32, i32]),
         "fp8_block_linear": (i32, [P, i32, i32, i32, P, P, P, P, P, P, sz, P]),
         "fp8_block_linear_workspace_size": (sz, [i32, i32, i32]),
+        "fp8_linear": (i32, [P, P, i32, i32, i32, P, P, P, P, sz, P]),
+        "fp8_linear_workspace_size": (sz, [i32, i32, i32]),
         "w4a8_device_error": (i32, [P, P, P]),
         "w4a8_set_profile_events": (i32, [P, i32]),
     }
@@ -110,6 +112,10 @@ def moe_route_workspace_size(T, E, k) -> int:
 
 def moe_route_gate_workspace_size(T, H, E, k) -> int:
     return int(_load().moe_route_gate_workspace_size(T, H, E, k))
+
+
+def fp8_linear_workspace_size(M, N, K) -> int:
+    return int(_load().fp8_linear_workspace_size(M, N, K))
 
 
 def fp8_block_linear_workspace_size(M, N, K) -> int:
@@ -208,6 +214,22 @@ def moe_w4a8_forward(x_e4m3, a1_scale, w_gu, s_gu, w_d, s_d, a2_scale, act: int,
         _ptr(a2_scale), int(act), _ptr(route.topk_ids), _ptr(route.topk_w), _ptr(route.counts),
         _ptr(route.offsets), _ptr(route.sorted_ids), _ptr(route.inv_perm), _ptr(out), _ptr(ws),
         ws.numel(), _stream(stream)))
+    return out
+
+
+def fp8_linear(x_e4m3, x_scale, w_e4m3, w_scale, out=None, ws=None, stream=None):
+    """Per-tensor FP8: E4M3 x [M, K] (scale [1]) x E4M3 W [N, K] (scale [1]) -> bf16 y [M, N].
+    A workspace passed in must have been zero-filled before its first use here."""
+    x = _u8(x_e4m3)
+    w = _u8(w_e4m3)
+    M, K = x.shape
+    N = w.shape[0]
+    dev = x.device
+    out = out if out is not None else torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    if ws is None:
+        ws = torch.zeros(max(fp8_linear_workspace_size(M, N, K), 256), dtype=torch.uint8, device=dev)
+    _check(_load().fp8_linear(_ptr(x), _ptr(x_scale), M, N, K, _ptr(w), _ptr(w_scale), _ptr(out), _ptr(ws),
+                              ws.numel(), _stream(stream)))
     return out
 
 

@@ -176,6 +176,21 @@ static size_t blk_ws(int M, int N, int K, BlkWs* w, void* ws)
     return c.off;
 }
 
+// Per-tensor FP8 linear: split-K partials, then one counter per
+// (128-row weight tile, token tile) -- token tiles are at least 16 wide.
+struct FpWs {
+    float* ypart;
+    int* tile_cnt;
+};
+static size_t fp_ws(int M, int N, int K, FpWs* w, void* ws)
+{
+    Carver c(ws);
+    const int ks = fp8_ksplit_max(M, K);
+    w->ypart = c.take<float>(ks > 1 ? static_cast<size_t>(ks) * M * N * 4 : 0);
+    w->tile_cnt = c.take<int>(static_cast<size_t>(N / 128) * ((M + 15) / 16) * 4);
+    return c.off;
+}
+
 }  // namespace w4a8
 
 using namespace w4a8;
@@ -393,6 +408,48 @@ size_t fp8_block_linear_workspace_size(int M, int N, int K)
 {
     BlkWs w;
     return blk_ws(M, N, K, &w, nullptr);
+}
+
+size_t fp8_linear_workspace_size(int M, int N, int K)
+{
+    FpWs w;
+    return fp_ws(M, N, K, &w, nullptr);
+}
+
+int fp8_linear(const uint8_t* x_e4m3, const float* x_scale, int M, int N, int K, const uint8_t* w_e4m3,
+               const float* w_scale, uint16_t* y_bf16, void* ws, size_t ws_bytes, void* stream)
+{
+    if (!x_e4m3 || !x_scale || !w_e4m3 || !w_scale || !y_bf16)
+        return W4A8_ERR_NULL;
+    if (M < 1 || N < 128 || N % 128 != 0 || K < 128 || K % 128 != 0)
+        return W4A8_ERR_SHAPE;
+    const void* ptrs[] = {x_e4m3, w_e4m3, y_bf16};
+    for (const void* p : ptrs)
+        if (!aligned16(p))
+            return W4A8_ERR_ALIGN;
+    if (!ws || ws_bytes < fp8_linear_workspace_size(M, N, K))
+        return W4A8_ERR_WORKSPACE;
+    if (!aligned16(ws))
+        return W4A8_ERR_ALIGN;
+    int sms;
+    if (int st = current_device(&sms))
+        return st;
+    FpWs w;
+    fp_ws(M, N, K, &w, ws);
+    FpLaunch L;
+    L.M = M;
+    L.N = N;
+    L.K = K;
+    L.x = x_e4m3;
+    L.sx = x_scale;
+    L.w = w_e4m3;
+    L.sw = w_scale;
+    L.y = y_bf16;
+    L.ypart = w.ypart;
+    L.tile_cnt = w.tile_cnt;
+    L.err = static_cast<uint32_t*>(ws);
+    const FpConfig cfg = fp8_pick_config(M, N, K, sms);
+    return launch_fp8_linear(L, cfg, sms, static_cast<cudaStream_t>(stream)) == kOK ? W4A8_OK : W4A8_ERR_LAUNCH;
 }
 
 int fp8_block_linear(const uint16_t* x_bf16, int M, int N, int K, const uint8_t* w_e4m3,

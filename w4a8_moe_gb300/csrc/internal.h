@@ -94,6 +94,20 @@ struct BlkLaunch {
 };
 int launch_block_gemm(const BlkLaunch& L, const BlkConfig& cfg, int num_sms, cudaStream_t s);
 
+// ---- fp8_linear.cu
+struct FpConfig {
+    int bn;
+    int ksplit;
+};
+FpConfig fp8_pick_config(int M, int N, int K, int num_sms);
+int fp8_ksplit_max(int M, int K);
+struct FpLaunch {
+    int M, N, K;
+    const uint8_t* x; const float* sx; const uint8_t* w; const float* sw; uint16_t* y;
+    float* ypart; int* tile_cnt; uint32_t* err;
+};
+int launch_fp8_linear(const FpLaunch& L, const FpConfig& cfg, int num_sms, cudaStream_t s);
+
 // ---- api.cu (tensor-map encoding through the driver entry point)
 bool encode_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
                    uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows,
