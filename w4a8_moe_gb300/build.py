@@ -59,6 +59,10 @@ def build(verbose: bool = False, extra=()) -> str:
             r = f.result()
             if verbose or r.returncode != 0:
                 sys.stderr.write(r.stdout + r.stderr)
+            else:   # register spills and other warnings are always shown
+                for line in (r.stdout + r.stderr).splitlines():
+                    if "warning" in line:
+                        sys.stderr.write(line + "\n")
             if r.returncode != 0:
                 raise RuntimeError(f"nvcc failed: {' '.join(j)}")
     if jobs or not os.path.exists(LIB):

@@ -116,6 +116,9 @@ __global__ void __launch_bounds__(384, 1)
 {
     using Tr = BlkTraits<BN, PST>;
     constexpr int NBUF = Tr::kNbuf;
+    // token tiles of 128 are used only without a K split (the host picks
+    // ksplit = 1 for them), so their reduction needs no register array
+    constexpr int kRed = BN >= 128 ? 1 : kBlkMaxKsplit;
     constexpr int NS = Tr::kNs;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -381,23 +384,33 @@ __global__ void __launch_bounds__(384, 1)
                 // fastest: coalesced); each requests all of an output's split
                 // partials before adding them in split order
                 const int mrows = min(BN, p.M - mt * BN);
-#pragma unroll 4
-                for (int o = threadIdx.x - 128; o < 128 * mrows; o += 256) {
-                    const int m = mt * BN + o / 128;
-                    const int nn = nb * 128 + (o & 127);
-                    const float* src = p.ypart + static_cast<int64_t>(m) * p.N + nn;
-                    const int64_t step = static_cast<int64_t>(p.M) * p.N;
-                    float v[kBlkMaxKsplit];
+                const int64_t step = static_cast<int64_t>(p.M) * p.N;
+                // 4 consecutive outputs per item (16-byte loads), every split
+                // of an item requested before its sum, splits added in order
+#pragma unroll 2
+                for (int o = threadIdx.x - 128; o < 32 * mrows; o += 256) {
+                    const int m = mt * BN + (o >> 5);
+                    const int nn = nb * 128 + (o & 31) * 4;
+                    const float4* src = reinterpret_cast<const float4*>(p.ypart + static_cast<int64_t>(m) * p.N + nn);
+                    float4 vv[kRed];
 #pragma unroll
-                    for (int s = 0; s < kBlkMaxKsplit; ++s)
+                    for (int s = 0; s < kRed; ++s)
                         if (s < p.ksplit)
-                            v[s] = __ldcg(src + s * step);
-                    float sum = 0.0f;
+                            vv[s] = __ldcg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(src) + s * step));
+                    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                    for (int s = 0; s < kBlkMaxKsplit; ++s)
-                        if (s < p.ksplit)
-                            sum += v[s];
-                    p.y[static_cast<int64_t>(m) * p.N + nn] = float_to_bf16_bits(sum);
+                    for (int s = 0; s < kRed; ++s) {
+                        if (s < p.ksplit) {
+                            sum.x += vv[s].x;
+                            sum.y += vv[s].y;
+                            sum.z += vv[s].z;
+                            sum.w += vv[s].w;
+                        }
+                    }
+                    uint2 ob;
+                    ob.x = float_to_bf16_bits(sum.x) | (static_cast<uint32_t>(float_to_bf16_bits(sum.y)) << 16);
+                    ob.y = float_to_bf16_bits(sum.z) | (static_cast<uint32_t>(float_to_bf16_bits(sum.w)) << 16);
+                    *reinterpret_cast<uint2*>(p.y + static_cast<int64_t>(m) * p.N + nn) = ob;
                 }
             }
         }
@@ -503,6 +516,8 @@ int launch_block_gemm(const BlkLaunch& L, const BlkConfig& cfg, int num_sms, cud
     p.tile_cnt = L.tile_cnt;
     p.y = L.y;
     p.err = L.err;
+    if (BN >= 128 && cfg.ksplit > 1)
+        return kErrLaunch;   // not produced by blk_pick_config
     const int64_t tiles = static_cast<int64_t>(p.nb_count) * p.mt_count * p.ksplit;
     const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
     switch (BN) {

@@ -310,22 +310,32 @@ __global__ void __launch_bounds__(384, 1)
             if (*s_last) {
                 const int mrows = min(BN, p.M - mt * BN);
                 const int64_t step = static_cast<int64_t>(p.M) * p.N;
-#pragma unroll 4
-                for (int o = threadIdx.x - 128; o < 128 * mrows; o += 256) {
-                    const int m = mt * BN + o / 128;
-                    const int nn = nb * 128 + (o & 127);
-                    const float* src = p.ypart + static_cast<int64_t>(m) * p.N + nn;
-                    float vv[kFpMaxKsplit];
+                // 4 consecutive outputs per item (16-byte loads), every split
+                // of an item requested before its sum, splits added in order
+#pragma unroll 2
+                for (int o = threadIdx.x - 128; o < 32 * mrows; o += 256) {
+                    const int m = mt * BN + (o >> 5);
+                    const int nn = nb * 128 + (o & 31) * 4;
+                    const float4* src = reinterpret_cast<const float4*>(p.ypart + static_cast<int64_t>(m) * p.N + nn);
+                    float4 vv[kFpMaxKsplit];
 #pragma unroll
                     for (int s = 0; s < kFpMaxKsplit; ++s)
                         if (s < p.ksplit)
-                            vv[s] = __ldcg(src + s * step);
-                    float sum = 0.0f;
+                            vv[s] = __ldcg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(src) + s * step));
+                    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                    for (int s = 0; s < kFpMaxKsplit; ++s)
-                        if (s < p.ksplit)
-                            sum += vv[s];
-                    p.y[static_cast<int64_t>(m) * p.N + nn] = float_to_bf16_bits(sum * scale);
+                    for (int s = 0; s < kFpMaxKsplit; ++s) {
+                        if (s < p.ksplit) {
+                            sum.x += vv[s].x;
+                            sum.y += vv[s].y;
+                            sum.z += vv[s].z;
+                            sum.w += vv[s].w;
+                        }
+                    }
+                    uint2 ob;
+                    ob.x = float_to_bf16_bits(sum.x * scale) | (static_cast<uint32_t>(float_to_bf16_bits(sum.y * scale)) << 16);
+                    ob.y = float_to_bf16_bits(sum.z * scale) | (static_cast<uint32_t>(float_to_bf16_bits(sum.w * scale)) << 16);
+                    *reinterpret_cast<uint2*>(p.y + static_cast<int64_t>(m) * p.N + nn) = ob;
                 }
                 if (threadIdx.x == 128)
                     p.tile_cnt[nb * p.mt_count + mt] = 0;   // zero for the next call
