@@ -7,14 +7,17 @@
 // node", Motivation: INT4 weights lower the memory bandwidth of decoding, the
 // FP8 tensor cores do the math.
 //
-// Grouped GEMM design (one persistent CTA per SM, 12 warps):
-//   warp 0      TMA producer: packed INT4 weight tile [128 rows x KC/2 bytes]
-//               and the expert's activation tile [BN tokens x KC] per stage.
-//   warp 1      TMEM owner + single-thread tcgen05.mma issuer.
-//   warps 4-7   converters: thread r owns A row r; it turns its packed
-//               nibbles into E4M3 bytes in the 128-byte-swizzled K-major layout
-//               the MMA reads.
-//   warps 8-11  epilogue: tcgen05.ld of the fp32 accumulator (lane = weight
+// Grouped GEMM design (one persistent CTA per SM, 8 + NCONV warps):
+//   warp 0      TMA producer of the packed INT4 weight tiles [128 rows x KC/2
+//               bytes] into the W ring (starts before the dependency wait).
+//   warp 2      TMA producer of the expert's activation tiles [BN x KC] into
+//               the X ring.
+//   warps 1, 3  TMEM owner and the MMA-issuing thread(s): with two issuers
+//               they take alternate stages into separate partial sums.
+//   warps 4..   converters: thread r owns A row r; it turns its packed nibbles
+//               into E4M3 bytes, in TMEM (tcgen05.st) for token tiles up to 128,
+//               else in the 128-byte-swizzled K-major shared-memory layout.
+//   last 4      epilogue: tcgen05.ld of the fp32 accumulators (lane = weight
 //               row, column = token), scales, activation, stores.
 // The MMA runs "swapped": M = 128 weight rows, N = the expert's tokens, so a
 // decode step with a handful of tokens per expert still uses M = 128 and the
@@ -98,8 +101,16 @@ struct TileInfo {
     int e, rt, tt, ks, tok0, ntok;
 };
 
+// Tile t of the CTA-shared tile list -> (expert, 128-row weight tile, token
+// tile, K split). Tiles run in expert order. Inside an expert, gate_up walks
+// weight rows outermost (the expert's gathered activations are small and stay
+// in L2 while its weight tiles stream once); down walks token tiles outermost,
+// so the CTAs working at the same time share a few token tiles of the
+// intermediate activation (which, for a long prefill, is far larger than L2)
+// and stream the weight rows, whose deeper ring hides HBM latency.
+template <int MODE>
 __device__ __forceinline__ TileInfo decode_tile(int t, const int* s_cnt, const int* s_off,
-                                                const int* s_pre, int E, int BN, int ksplit)
+                                                const int* s_pre, int E, int BN, int ksplit, int rt_count)
 {
     TileInfo ti;
     int e = 0;
@@ -108,12 +119,20 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const int* s_cnt, const i
     const int local = t - s_pre[e];
     const int c = s_cnt[e];
     const int ntt = (c + BN - 1) / BN;
-    const int per_rt = ntt * ksplit;
     ti.e = e;
-    ti.rt = local / per_rt;
-    const int r2 = local - ti.rt * per_rt;
-    ti.tt = r2 / ksplit;
-    ti.ks = r2 - ti.tt * ksplit;
+    if (MODE == 0) {
+        const int per_rt = ntt * ksplit;
+        ti.rt = local / per_rt;
+        const int r2 = local - ti.rt * per_rt;
+        ti.tt = r2 / ksplit;
+        ti.ks = r2 - ti.tt * ksplit;
+    } else {
+        const int per_tt = rt_count * ksplit;
+        ti.tt = local / per_tt;
+        const int r2 = local - ti.tt * per_tt;
+        ti.rt = r2 / ksplit;
+        ti.ks = r2 - ti.rt * ksplit;
+    }
     ti.tok0 = s_off[e] + ti.tt * BN;
     ti.ntok = min(BN, c - ti.tt * BN);
     return ti;
@@ -268,7 +287,7 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
             uint32_t last_par = 0;     // bit s: parity of the last fill of slot s
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const TileInfo ti = decode_tile(t, s_cnt, s_off, s_pre, p.E, BN, p.ksplit);
+                const TileInfo ti = decode_tile<MODE>(t, s_cnt, s_off, s_pre, p.E, BN, p.ksplit, p.rt_count);
                 for (int kb = 0; kb < p.kblocks; ++kb) {
                     if (!mbar_wait_or_abort(smem_u32(&freeb[s]), ph ^ 1u, s_abort)) {
                         ok = false;
@@ -330,7 +349,7 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
             int it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
-                const TileInfo ti = decode_tile(t, s_cnt, s_off, s_pre, p.E, BN, p.ksplit);
+                const TileInfo ti = decode_tile<MODE>(t, s_cnt, s_off, s_pre, p.E, BN, p.ksplit, p.rt_count);
                 const int nmma = max(16, (ti.ntok + 15) & ~15);
                 const uint32_t idesc = idesc_e4m3_f32(128, nmma);
                 const int d = it & 1;
@@ -477,7 +496,7 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
         int it = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
-            const TileInfo ti = decode_tile(t, s_cnt, s_off, s_pre, p.E, BN, p.ksplit);
+            const TileInfo ti = decode_tile<MODE>(t, s_cnt, s_off, s_pre, p.E, BN, p.ksplit, p.rt_count);
             const int d = it & 1;
             const uint32_t use = static_cast<uint32_t>(it >> 1);
             if (!mbar_wait_or_abort(smem_u32(&accfull[d]), use & 1u, s_abort)) {
