@@ -51,7 +51,10 @@ struct BlkTraits {
     static constexpr int kSBytes = BN * 4;                               // one scale slot's copy
     static constexpr int kSStride = ((kSBytes + 127) / 128) * 128;       // TMA destinations: 128-byte aligned
     static constexpr int kData = PST * kStage + ((kNs * kSStride + 1023) / 1024) * 1024;
-    static constexpr int kBars = 3 * PST + 2 * kNs + 2 * kNbuf + 1;
+    static constexpr int kBars = 3 * PST + 2 * kNs + 2 * kNbuf + 2;
+    // the two MMA-issuing threads take alternate K-blocks: every ring slot and
+    // partial buffer must always belong to the same thread (parity waits)
+    static_assert(PST % 2 == 0 && kNbuf % 2 == 0, "even ring depths for two issuers");
     static constexpr int kSmem = 1024 + kData + kBars * 8 + 32;
     static constexpr int kTmemNeed = kNbuf * BN;
     static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
@@ -63,6 +66,31 @@ struct BlkTraits {
     static_assert(kSmem <= 232448, "shared memory budget");
     static_assert(kTmemNeed <= 512, "tensor memory budget");
 };
+
+// Packed pairs of fp32 (low word = first element) and the sm_100-family
+// paired arithmetic on them; each lane rounds exactly like the scalar op.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
 
 // Barrier over `nthreads` threads (named barrier `id`) that returns whether
 // any of them passed pred = true.
@@ -133,7 +161,7 @@ __global__ void __launch_bounds__(384, 1)
     uint64_t* dfull = sfree + NS;       // partial product ready  [NBUF]
     uint64_t* dempty = dfull + NBUF;    // partial buffer folded  [NBUF]
     uint64_t* drain = dempty + NBUF;
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain + 1);
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain + 2);   // one drain barrier per issuer
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
     int* s_last = reinterpret_cast<int*>(s_tmem + 2);
 
@@ -154,7 +182,8 @@ __global__ void __launch_bounds__(384, 1)
             mbar_init(smem_u32(&dfull[i]), 1);
             mbar_init(smem_u32(&dempty[i]), 8);
         }
-        mbar_init(smem_u32(drain), 1);
+        mbar_init(smem_u32(&drain[0]), 1);
+        mbar_init(smem_u32(&drain[1]), 1);
         fence_mbar_init();
         *s_abort = 0;
     }
@@ -248,15 +277,26 @@ __global__ void __launch_bounds__(384, 1)
                         mbar_wait(smem_u32(&sfull[s]), (s_last_par >> s) & 1u);
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == 1 || warp == 3) {
+        // ------------------------------------------------------------ MMA issuers
+        // Every K-block has its own partial buffer, so two threads can issue:
+        // warp 1 takes the even K-blocks of the CTA's sequence, warp 3 the odd
+        // ones, which hides each thread's barrier waits behind the other's MMAs.
         if (lane == 0) {
+            const int me = (warp == 1) ? 0 : 1;
             const uint32_t idesc = idesc_e4m3_f32(128, BN);
             int ps = 0;
             uint32_t ph = 0, kc = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 for (int kb = 0; kb < p.kb_per_split; ++kb, ++kc) {
+                    if (static_cast<int>(kc & 1u) != me) {
+                        if (++ps == PST) {
+                            ps = 0;
+                            ph ^= 1u;
+                        }
+                        continue;
+                    }
                     const int d = static_cast<int>(kc % NBUF);
                     const uint32_t use = kc / NBUF;
                     if (!mbar_wait_or_abort(smem_u32(&dempty[d]), (use & 1u) ^ 1u, s_abort) ||
@@ -283,8 +323,8 @@ __global__ void __launch_bounds__(384, 1)
             }
             if (!ok) {
                 fail();
-                umma_commit(smem_u32(drain));
-                mbar_wait(smem_u32(drain), 0);
+                umma_commit(smem_u32(&drain[me]));
+                mbar_wait(smem_u32(&drain[me]), 0);
             }
         }
     } else if (warp >= 4) {
@@ -299,10 +339,12 @@ __global__ void __launch_bounds__(384, 1)
         bool ok = true;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
             const int nb = t / per_nb, r = t % per_nb, mt = r / p.ksplit, ks = r % p.ksplit;
-            float acc[Tr::kHalf];
+            // column pairs, folded with packed fp32x2 arithmetic (each lane of a
+            // pair rounds exactly like the scalar fmaf(p, xs * ws, acc))
+            uint64_t acc2[Tr::kHalf / 2];
 #pragma unroll
-            for (int c = 0; c < Tr::kHalf; ++c)
-                acc[c] = 0.0f;
+            for (int c = 0; c < Tr::kHalf / 2; ++c)
+                acc2[c] = 0ull;
             for (int kb = 0; kb < p.kb_per_split; ++kb, ++kc) {
                 const int d = static_cast<int>(kc % NBUF);
                 const uint32_t use = kc / NBUF;
@@ -314,6 +356,7 @@ __global__ void __launch_bounds__(384, 1)
                 tc_fence_after();
                 const int g = ks * p.kb_per_split + kb;
                 const float ws = __ldg(p.wsi + static_cast<int64_t>(nb) * p.KB + g);
+                const uint64_t ws2 = f2_pack(ws, ws);
                 const float* xs = reinterpret_cast<const float*>(sring + ss * Tr::kSStride);
                 const uint32_t tb = tmem + (static_cast<uint32_t>(q * 32) << 16) +
                                     static_cast<uint32_t>(d * BN + c0);
@@ -322,11 +365,13 @@ __global__ void __launch_bounds__(384, 1)
                     uint32_t v[Tr::kChunk];
                     tmem_ld_cols<Tr::kChunk>(tb + ch * Tr::kChunk, v);
                     tmem_ld_wait();
+                    const uint64_t* xs2 = reinterpret_cast<const uint64_t*>(xs + c0 + ch * Tr::kChunk);
 #pragma unroll
-                    for (int c = 0; c < Tr::kChunk; ++c)
-                        acc[ch * Tr::kChunk + c] =
-                            fmaf(__uint_as_float(v[c]), xs[c0 + ch * Tr::kChunk + c] * ws,
-                                 acc[ch * Tr::kChunk + c]);
+                    for (int c = 0; c < Tr::kChunk / 2; ++c) {
+                        const uint64_t sc = f2_mul(xs2[c], ws2);
+                        const uint64_t pv = f2_pack(__uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1]));
+                        acc2[ch * Tr::kChunk / 2 + c] = f2_fma(pv, sc, acc2[ch * Tr::kChunk / 2 + c]);
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -339,6 +384,10 @@ __global__ void __launch_bounds__(384, 1)
                     sph ^= 1u;
                 }
             }
+            float acc[Tr::kHalf];
+#pragma unroll
+            for (int c = 0; c < Tr::kHalf / 2; ++c)
+                f2_unpack(acc2[c], acc[2 * c], acc[2 * c + 1]);
             const int n = nb * 128 + q * 32 + lane;
             if (p.ksplit == 1) {
                 if (!ok)
