@@ -44,6 +44,18 @@ def test_shapes_and_tails(T, H, I, E, k, act):
     run_case(case, what=f"T{T} H{H} I{I} E{E} k{k}")
 
 
+@pytest.mark.parametrize("T,H,I,E,k", [
+    (1, 4096, 14336, 8, 2),   # Mixtral-shaped single token: 2 of 8 experts active
+    (3, 2048, 4096, 8, 2),    # 6 assignments over 8 experts
+    (4, 2048, 4096, 16, 4),   # 16 assignments, 16 experts
+])
+def test_stream_k_down_projection(T, H, I, E, k):
+    """T*k <= E: the down GEMM takes equal K-block ranges per CTA; tiles cut
+    by CTA boundaries are summed from several partial slots."""
+    case = MoECase(T, H, I, E, k, 0, seed=41 + T)
+    run_case(case, what=f"stream-K T{T} H{H} I{I} E{E} k{k}")
+
+
 def test_empty_experts_and_one_hot_expert():
     T, E = 50, 8
     logits = torch.randn(T, E, generator=torch.Generator().manual_seed(3))

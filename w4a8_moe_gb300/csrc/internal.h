@@ -61,7 +61,9 @@ constexpr int kMaxKsplit = 16;   // largest split of the down projection's K
 struct MoeConfig {
     int bn;        // token tile (MMA N upper bound)
     int kc;        // K elements per pipeline stage
-    int ksplit;    // split of the down projection's K
+    int ksplit;    // split of the down projection's K (round-robin tiles)
+    int streamk;   // 1: the down GEMM takes equal K-block ranges per CTA
+    int nslots;    // stream-K partial slots per output
 };
 MoeConfig moe_pick_config(int T, int H, int I, int E, int k, int num_sms);
 int moe_ksplit_max(int T, int k);

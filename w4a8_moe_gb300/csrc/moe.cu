@@ -54,7 +54,9 @@ struct MoeGemmParams {
     uint8_t* hq;             // [A, I]
     unsigned long long* s0h; // [A] sum_i 512*dec(hq), accumulated by atomics
     // down epilogue
-    float* ypart;            // [ksplit, A, H] raw accumulator (before shift removal)
+    float* ypart;            // [ksplit or nslots, A, H] raw accumulator (before shift removal)
+    int streamk;             // down only: equal stage ranges per CTA (see WorkIter)
+    int nslots;              // stream-K: partial slots per output (unused ones zeroed)
     uint32_t* err;
 };
 
@@ -137,6 +139,67 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const int* s_cnt, const i
     ti.ntok = min(BN, c - ti.tt * BN);
     return ti;
 }
+
+// The CTA's work as a sequence of segments (tile t, first K-block kb0, nkb
+// K-blocks, partial slot). Round robin: tiles blockIdx.x, +gridDim.x, ...,
+// whole (slot = K split). Stream-K (down GEMM of decode-sized layers): the
+// K-blocks of all tiles form one sequence of S stages and CTA c takes
+// [c*S/G, (c+1)*S/G), so every CTA streams the same number of weight bytes; a
+// tile cut by CTA boundaries yields one segment per CTA, and a segment's slot
+// is the number of boundaries before it inside its tile.
+struct WorkIter {
+    int t, kb0, nkb, slot;
+    bool last;            // the segment ends its tile
+    int total, kbt, stride;
+    bool sk;
+    int64_t s, s_end, S, G;
+    __device__ __forceinline__ int64_t owner(int64_t x) const { return ((x + 1) * G - 1) / S; }
+    __device__ __forceinline__ void load()
+    {
+        if (sk) {
+            if (s >= s_end) {
+                t = total;
+                return;
+            }
+            t = static_cast<int>(s / kbt);
+            kb0 = static_cast<int>(s - static_cast<int64_t>(t) * kbt);
+            const int64_t left = s_end - s;
+            nkb = static_cast<int>(left < kbt - kb0 ? left : kbt - kb0);
+            slot = static_cast<int>(owner(s) - owner(static_cast<int64_t>(t) * kbt));
+            last = (kb0 + nkb == kbt);
+        }
+    }
+    __device__ __forceinline__ void init(int total_, int kbt_, bool streamk)
+    {
+        total = total_;
+        kbt = kbt_;
+        sk = streamk;
+        stride = gridDim.x;
+        if (sk) {
+            S = static_cast<int64_t>(total) * kbt;
+            G = gridDim.x;
+            s = S * blockIdx.x / G;
+            s_end = S * (blockIdx.x + 1) / G;
+            load();
+        } else {
+            t = blockIdx.x;
+            kb0 = 0;
+            nkb = kbt;
+            slot = 0;
+            last = true;
+        }
+    }
+    __device__ __forceinline__ bool valid() const { return t < total; }
+    __device__ __forceinline__ void next()
+    {
+        if (sk) {
+            s += nkb;
+            load();
+        } else {
+            t += stride;
+        }
+    }
+};
 
 // Nibbles -> E4M3 operand bytes worth (q + 8) * 2^-9. The two output words
 // hold the weights of one packed word in the order [0,2,4,6 | 1,3,5,7]: the
@@ -286,9 +349,11 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
             uint32_t issued = 0;       // bit s: slot s was filled at least once
             uint32_t last_par = 0;     // bit s: parity of the last fill of slot s
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            WorkIter wi;
+            for (wi.init(total, p.kblocks, p.streamk != 0); wi.valid() && ok; wi.next()) {
+                const int t = wi.t;
                 const TileInfo ti = decode_tile<MODE>(t, s_cnt, s_off, s_pre, p.E, BN, p.ksplit, p.rt_count);
-                for (int kb = 0; kb < p.kblocks; ++kb) {
+                for (int kb = wi.kb0; kb < wi.kb0 + wi.nkb; ++kb) {
                     if (!mbar_wait_or_abort(smem_u32(&freeb[s]), ph ^ 1u, s_abort)) {
                         ok = false;
                         break;
@@ -348,8 +413,9 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
             uint32_t g = 0;
             int it = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
-                const TileInfo ti = decode_tile<MODE>(t, s_cnt, s_off, s_pre, p.E, BN, p.ksplit, p.rt_count);
+            WorkIter wi;
+            for (wi.init(total, p.kblocks, p.streamk != 0); wi.valid() && ok; wi.next(), ++it) {
+                const TileInfo ti = decode_tile<MODE>(wi.t, s_cnt, s_off, s_pre, p.E, BN, p.ksplit, p.rt_count);
                 const int nmma = max(16, (ti.ntok + 15) & ~15);
                 const uint32_t idesc = idesc_e4m3_f32(128, nmma);
                 const int d = it & 1;
@@ -361,7 +427,7 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                 tc_fence_after();
                 const uint32_t dt = tmem + static_cast<uint32_t>((d * NISS + me) * BN);
                 bool first = true;
-                for (int kb = 0; kb < p.kblocks; ++kb, ++g) {
+                for (int kb = 0; kb < wi.nkb; ++kb, ++g) {
                     if (static_cast<int>(g % NISS) == me) {
                         if (!mbar_wait_or_abort(smem_u32(&afull[x]), ph, s_abort)) {
                             ok = false;
@@ -420,8 +486,9 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
         uint32_t wph = 0, xph = 0;
         uint32_t g = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            for (int kb = 0; kb < p.kblocks; ++kb, ++g) {
+        WorkIter wi;
+        for (wi.init(total, p.kblocks, p.streamk != 0); wi.valid() && ok; wi.next()) {
+            for (int kb = 0; kb < wi.nkb; ++kb, ++g) {
                 if (static_cast<int>(g % Tr::kPar) == par) {
                     if (!mbar_wait_or_abort(smem_u32(&wfull[w]), wph, s_abort) ||
                         !mbar_wait_or_abort(smem_u32(&bfull[x]), xph, s_abort)) {
@@ -495,8 +562,9 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
         uint32_t gsum = 0;   // global stage index of the tile's first stage
         int it = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
-            const TileInfo ti = decode_tile<MODE>(t, s_cnt, s_off, s_pre, p.E, BN, p.ksplit, p.rt_count);
+        WorkIter wi;
+        for (wi.init(total, p.kblocks, p.streamk != 0); wi.valid() && ok; wi.next(), ++it) {
+            const TileInfo ti = decode_tile<MODE>(wi.t, s_cnt, s_off, s_pre, p.E, BN, p.ksplit, p.rt_count);
             const int d = it & 1;
             const uint32_t use = static_cast<uint32_t>(it >> 1);
             if (!mbar_wait_or_abort(smem_u32(&accfull[d]), use & 1u, s_abort)) {
@@ -508,9 +576,9 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                                    static_cast<uint32_t>(d * NISS * BN);
             // partial sum of issuer i is valid when the issuer had a stage in
             // this tile: always when the tile has two or more stages
-            const bool v0 = NISS == 1 || p.kblocks >= 2 || (gsum % NISS) == 0;
-            const bool v1 = NISS == 2 && (p.kblocks >= 2 || (gsum % NISS) == 1);
-            gsum += p.kblocks;
+            const bool v0 = NISS == 1 || wi.nkb >= 2 || (gsum % NISS) == 0;
+            const bool v1 = NISS == 2 && (wi.nkb >= 2 || (gsum % NISS) == 1);
+            gsum += wi.nkb;
             auto load_acc = [&](int c, uint32_t (&v)[32]) {
                 if (v0) {
                     tmem_ld32(tbase + c, v);
@@ -584,14 +652,25 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                 }
             } else {
                 const int n = ti.rt * 128 + q * 32 + lane;
-                float* yb = p.ypart + (static_cast<int64_t>(ti.ks) * p.A + ti.tok0) * p.H + n;
+                int slot = p.streamk ? wi.slot : ti.ks;
+                if (p.streamk && slot >= p.nslots) {   // excluded by the host's bound
+                    set_error(p.err, kErrBitTimeout);
+                    slot = -1;
+                }
+                float* yb = p.ypart + (static_cast<int64_t>(slot) * p.A + ti.tok0) * p.H + n;
+                if (p.streamk && wi.last) {
+                    // the tile's last segment: slots no CTA writes hold zero
+                    for (int sl = wi.slot + 1; sl < p.nslots; ++sl)
+                        for (int col = 0; col < ti.ntok; ++col)
+                            p.ypart[(static_cast<int64_t>(sl) * p.A + ti.tok0 + col) * p.H + n] = 0.0f;
+                }
                 for (int ch = 0; ch < nchunks; ++ch) {
                     uint32_t v[32];
                     load_acc(ch * 32, v);
 #pragma unroll
                     for (int cc = 0; cc < 32; ++cc) {
                         const int col = ch * 32 + cc;
-                        if (col < ti.ntok)
+                        if (col < ti.ntok && slot >= 0)
                             yb[static_cast<int64_t>(col) * p.H] = __uint_as_float(v[cc]);
                     }
                 }
@@ -773,6 +852,26 @@ MoeConfig moe_pick_config(int T, int H, int I, int E, int k, int num_sms)
         }
     }
     c.ksplit = best;
+    // With at most E assignments (T*k <= E) most experts may be idle, and the
+    // split above (chosen for E active experts) would leave SMs without work:
+    // the down GEMM then runs stream-K, equal K-block ranges per CTA over the
+    // tiles that exist, at most `nslots` segments per tile. (Measured: with
+    // every expert active it is no faster than the split.) The slot bound
+    // takes the fewest active experts (k): a CTA's range is then
+    // S/G >= k * (H/128) * K-blocks / G stages.
+    c.streamk = 0;
+    c.nslots = 0;
+    if (T <= 128 && static_cast<int64_t>(T) * k <= E) {
+        const int rt = H / 128;
+        const int need = (num_sms + k * rt - 1) / (k * rt) + 2;
+        // every CTA range must be non-empty (then the CTA boundaries are
+        // distinct and a tile's segments take consecutive slots)
+        const bool ranges_nonempty = static_cast<int64_t>(k) * rt * kblocks >= num_sms;
+        if (need <= kmax && ranges_nonempty) {
+            c.streamk = 1;
+            c.nslots = need;
+        }
+    }
     return c;
 }
 
@@ -869,10 +968,12 @@ int launch_moe_forward(const MoeLaunch& L, const MoeConfig& cfg, int num_sms, cu
     MoeGemmParams dn = g;
     dn.rows_per_expert = L.H;
     dn.rt_count = L.H / 128;
-    dn.ksplit = cfg.ksplit;
-    dn.kblocks = L.I / KC / cfg.ksplit;
-    tiles = static_cast<int64_t>(dn.rt_count) * tok_tiles_max * cfg.ksplit;
-    grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
+    dn.ksplit = cfg.streamk ? 1 : cfg.ksplit;
+    dn.kblocks = L.I / KC / dn.ksplit;
+    dn.streamk = cfg.streamk;
+    dn.nslots = cfg.nslots;
+    tiles = static_cast<int64_t>(dn.rt_count) * tok_tiles_max * dn.ksplit;
+    grid = cfg.streamk ? num_sms : static_cast<int>(tiles < num_sms ? tiles : num_sms);
     st = dispatch_gemm<1>(cfg, tw_d, tb_d, dn, grid, s);
     if (st != kOK)
         return st;
@@ -880,10 +981,12 @@ int launch_moe_forward(const MoeLaunch& L, const MoeConfig& cfg, int num_sms, cu
 
     const int64_t nthreads = static_cast<int64_t>(L.T) * (L.H / 4);
     // the register array of split partials is sized for the split in use
-    auto fin = cfg.ksplit == 1 ? moe_finalize_kernel<1>
-             : cfg.ksplit <= 4 ? moe_finalize_kernel<4> : moe_finalize_kernel<kMaxKsplit>;
+    const int parts = cfg.streamk ? cfg.nslots : cfg.ksplit;
+    auto fin = parts == 1 ? moe_finalize_kernel<1>
+             : parts <= 4 ? moe_finalize_kernel<4>
+             : parts <= 8 ? moe_finalize_kernel<8> : moe_finalize_kernel<kMaxKsplit>;
     if (launch_dependent(fin, dim3(static_cast<unsigned>((nthreads + 255) / 256)), dim3(256), 0, s,
-                         L.T, L.H, L.k, A, cfg.ksplit, L.ids, L.topk_w, L.inv, L.ypart,
+                         L.T, L.H, L.k, A, parts, L.ids, L.topk_w, L.inv, L.ypart,
                          static_cast<const unsigned long long*>(L.s0h), L.s_d, L.a2, L.out) != cudaSuccess)
         return kErrLaunch;
     mark(3);
