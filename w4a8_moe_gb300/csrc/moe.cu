@@ -60,30 +60,33 @@ struct MoeGemmParams {
     uint32_t* err;
 };
 
-template <int MODE, int BN, int KC, int NW, int NX, bool ATMEM, int NCONV, int NISS>
+template <int MODE, int BN, int KC, int NW, int NX, int NXT, int NCONV, int NISS>
 struct MoeTraits {
     static constexpr int kAtoms = KC / 128;                      // 128-byte K atoms of A and B
     static constexpr int kWBytes = 128 * KC / 2;                 // packed weights per stage
     static constexpr int kWBoxBytes = KC == 128 ? 64 : 128;      // bytes per row per TMA box
     static constexpr int kWBoxes = KC / 2 / kWBoxBytes;
     static constexpr int kBBytes = kAtoms * BN * 128;            // activations per stage
-    static constexpr int kABytes = ATMEM ? 0 : kAtoms * 128 * 128;  // unpacked A in smem
-    static constexpr int kXBytes = kBBytes + kABytes;
-    static constexpr int kACols = KC / 4;                        // unpacked A in TMEM
-    static constexpr int kData = NW * kWBytes + NX * kXBytes;
+    static constexpr int kXBytes = kBBytes;                      // X slot in shared memory: B
+    static constexpr int kASlot = kAtoms * 128 * 128;            // unpacked A of a shared-memory slot
+    static constexpr int kACols = KC / 4;                        // unpacked A of a TMEM slot
+    // X slots 0..NXT-1 keep their unpacked A in TMEM, slots NXT..NX-1 in
+    // shared memory (after the B tiles)
+    static constexpr int kData = NW * kWBytes + NX * kXBytes + (NX - NXT) * kASlot;
     static constexpr int kBars = 2 * NW + 3 * NX + 4 + 2;        // + drain barriers
     static constexpr int kCtrl = kBars * 8 + 16 + 4 * (256 + 260 + 260);
     static constexpr int kSmem = 1024 + kData + kCtrl;
     // two accumulator buffers (tile i / tile i+1), each with one partial sum
     // per MMA-issuing thread
     static constexpr int kDCols = 2 * NISS * BN;
-    static constexpr int kTmemNeed = kDCols + (ATMEM ? NX * kACols : 0);
+    static constexpr int kTmemNeed = kDCols + NXT * kACols;
     static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
                                    : kTmemNeed <= 256 ? 256 : 512;
     static constexpr int kThreads = 32 * (8 + NCONV);
     static constexpr int kEpi0 = 4 + NCONV;                      // first epilogue warp
     static constexpr int kPar = NCONV / 4;                       // converter warps per quadrant
-    static_assert(kWBytes % 1024 == 0 && kXBytes % 1024 == 0, "stage alignment");
+    static_assert(kWBytes % 1024 == 0 && kXBytes % 1024 == 0 && kASlot % 1024 == 0, "stage alignment");
+    static_assert(NXT >= 0 && NXT <= NX, "TMEM A slots");
     static_assert(kSmem <= 232448, "shared memory budget");
     static_assert(kTmemNeed <= 512, "tensor memory budget");
     static_assert(BN % 16 == 0 && BN <= 256, "token tile");
@@ -245,17 +248,18 @@ __device__ __forceinline__ float act_fn(float z, int act)
 // which both guarantees its A slot is free (bfull round r follows xfree round
 // r-1) and lets the MMA wait on afull alone: one wait and one commit per stage
 // in the single MMA thread.
-template <int MODE, int BN, int KC, int NW, int NX, bool ATMEM, int NCONV, int NISS>
+template <int MODE, int BN, int KC, int NW, int NX, int NXT, int NCONV, int NISS>
 __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b,
                     const MoeGemmParams p)
 {
-    using Tr = MoeTraits<MODE, BN, KC, NW, NX, ATMEM, NCONV, NISS>;
+    using Tr = MoeTraits<MODE, BN, KC, NW, NX, NXT, NCONV, NISS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
     uint8_t* wring = smem;
     uint8_t* xring = smem + NW * Tr::kWBytes;
+    uint8_t* aring = xring + NX * Tr::kXBytes;       // unpacked A of X slots NXT..NX-1
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Tr::kData);
     uint64_t* wfull = bars;
     uint64_t* wfree = wfull + NW;
@@ -323,7 +327,7 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
-    const uint32_t tmem_a = tmem + Tr::kDCols;   // A slots (ATMEM)
+    const uint32_t tmem_a = tmem + Tr::kDCols;   // A of X slots 0..NXT-1
     const int total = s_pre[p.E];
 
     auto fail = [&]() {
@@ -436,14 +440,16 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                         tc_fence_after();
                         const uint8_t* st = xring + x * Tr::kXBytes;
                         const uint64_t bd0 = desc_kmajor_sw128(smem_u32(st));
-                        const uint64_t ad0 = ATMEM ? 0 : desc_kmajor_sw128(smem_u32(st + Tr::kBBytes));
+                        const bool a_tmem = x < NXT;
+                        const uint64_t ad0 =
+                            a_tmem ? 0 : desc_kmajor_sw128(smem_u32(aring + (x - NXT) * Tr::kASlot));
 #pragma unroll
                         for (int kk = 0; kk < KC / 32; ++kk) {
                             const int atom = kk >> 2, sub = kk & 3;
                             // start-address field advances in 16-byte units
                             const uint64_t bd = bd0 + static_cast<uint64_t>((atom * BN * 128 + sub * 32) >> 4);
                             const uint32_t acc = (first && kk == 0) ? 0u : 1u;
-                            if (ATMEM) {
+                            if (a_tmem) {
                                 umma_f8_ta(dt, tmem_a + static_cast<uint32_t>(x * Tr::kACols + kk * 8), bd, idesc,
                                            acc);
                             } else {
@@ -514,12 +520,12 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                             unpack8(w4.z, o[8 * c4 + 4], o[8 * c4 + 5]);
                             unpack8(w4.w, o[8 * c4 + 6], o[8 * c4 + 7]);
                         }
-                        if (ATMEM) {
+                        if (x < NXT) {
                             tmem_st32(tmem_a + (static_cast<uint32_t>(q * 32) << 16) +
                                           static_cast<uint32_t>(x * Tr::kACols + half * 32),
                                       o);
                         } else {
-                            uint8_t* arow = xring + x * Tr::kXBytes + Tr::kBBytes + half * (128 * 128) + r * 128;
+                            uint8_t* arow = aring + (x - NXT) * Tr::kASlot + half * (128 * 128) + r * 128;
 #pragma unroll
                             for (int c16 = 0; c16 < 8; ++c16)
                                 *reinterpret_cast<uint4*>(arow + ((c16 ^ (r & 7)) << 4)) =
@@ -530,7 +536,7 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                     __syncwarp();
                     if (lane == 0)
                         mbar_arrive(smem_u32(&wfree[w]));
-                    if (ATMEM) {
+                    if (x < NXT) {
                         tmem_st_wait();
                         tc_fence_before();
                     } else {
@@ -875,12 +881,12 @@ MoeConfig moe_pick_config(int T, int H, int I, int E, int k, int num_sms)
     return c;
 }
 
-template <int MODE, int BN, int KC, int NW, int NX, bool ATMEM, int NCONV, int NISS>
+template <int MODE, int BN, int KC, int NW, int NX, int NXT, int NCONV, int NISS>
 static int launch_gemm(const CUtensorMap& tw, const CUtensorMap& tb, const MoeGemmParams& prm, int grid,
                        cudaStream_t s)
 {
-    using Tr = MoeTraits<MODE, BN, KC, NW, NX, ATMEM, NCONV, NISS>;
-    auto kern = moe_gemm_kernel<MODE, BN, KC, NW, NX, ATMEM, NCONV, NISS>;
+    using Tr = MoeTraits<MODE, BN, KC, NW, NX, NXT, NCONV, NISS>;
+    auto kern = moe_gemm_kernel<MODE, BN, KC, NW, NX, NXT, NCONV, NISS>;
     // attribute set on every launch: cheap, and correct for every device
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Tr::kSmem) != cudaSuccess)
         return kErrLaunch;
@@ -898,10 +904,10 @@ static int dispatch_gemm(const MoeConfig& cfg, const CUtensorMap& tw, const CUte
                          const MoeGemmParams& prm, int grid, cudaStream_t s)
 {
     switch (cfg.bn) {
-    case 32: return launch_gemm<MODE, 32, 256, 10, 6, true, 8, 2>(tw, tb, prm, grid, s);
-    case 64: return launch_gemm<MODE, 64, 256, 8, 4, true, 8, 2>(tw, tb, prm, grid, s);
-    case 128: return launch_gemm<MODE, 128, 256, 4, 4, true, 8, 1>(tw, tb, prm, grid, s);
-    default: return launch_gemm<MODE, 256, 128, 8, 3, false, 4, 1>(tw, tb, prm, grid, s);
+    case 32: return launch_gemm<MODE, 32, 256, 10, 6, 6, 8, 2>(tw, tb, prm, grid, s);
+    case 64: return launch_gemm<MODE, 64, 256, 8, 4, 4, 8, 2>(tw, tb, prm, grid, s);
+    case 128: return launch_gemm<MODE, 128, 256, 4, 4, 4, 8, 1>(tw, tb, prm, grid, s);
+    default: return launch_gemm<MODE, 256, 128, 8, 3, 0, 4, 1>(tw, tb, prm, grid, s);
     }
 }
 
