@@ -401,6 +401,37 @@ def run_suite(args):
         del st
         torch.cuda.empty_cache()
 
+    # Mixtral decode with the intermediate scale calibrated on the device per call
+    shape = synth.MOE_SHAPES["mixtral_decode"]
+    st = prepare_moe(shape, 0, dev)
+    T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
+    wsd = torch.zeros(lib.moe_w4a8_dynamic_workspace_size(T, H, I, E, k), dtype=torch.uint8, device=dev)
+    a2d = torch.empty(1, dtype=torch.float32, device=dev)
+
+    def dyn_step():
+        lib.moe_route(st["logits"], k, out=st["route"], ws=st["route_ws"])
+        lib.moe_w4a8_forward_dynamic(st["xq"], st["a1"], st["w_gu"], st["s_gu"], st["w_d"], st["s_d"],
+                                     shape.act, st["route"], out=st["out"], a2_out=a2d, ws=wsd)
+
+    res = {}
+    for name, fn in (("static", lambda: moe_step(lib, shape, st)), ("dynamic", dyn_step)):
+        for _ in range(20):
+            fn()
+        s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        s_ev.record()
+        for _ in range(1000):
+            fn()
+        e_ev.record()
+        torch.cuda.synchronize()
+        res[name] = s_ev.elapsed_time(e_ev) / 1000
+    assert lib.w4a8_device_error(wsd) == 0, "device error word set"
+    print(json.dumps({"suite": True, "workload": shape.name + ", intermediate scale static vs dynamic",
+                      "ms_per_step": res, "tokens_per_s": {n: T / (v * 1e-3) for n, v in res.items()},
+                      "dynamic_a2": a2d.item()}), flush=True)
+    del st
+    torch.cuda.empty_cache()
+
     # router gate fused with routing (one launch at decode) against the gate
     # product as a separate library matmul followed by moe_route
     for (T, H, E, k) in ((32, 4096, 8, 2), (32, 6144, 8, 2)):

@@ -174,6 +174,26 @@ int moe_w4a8_forward(const uint8_t* x_e4m3, const float* a1_scale, int T, int H,
 size_t moe_w4a8_workspace_size(int T, int H, int I, int E, int k);
 
 /*
+ * moe_w4a8_forward_dynamic -- moe_w4a8_forward with the intermediate
+ * activation's scale calibrated on the device for every call instead of read:
+ *   a2 = max |h_i| / 448 over every assignment and i of the call (1 when all
+ *        h are zero), written to a2_out [1] fp32 (device), then used exactly
+ *        as the static a2 of moe_w4a8_forward.
+ * PR #4152 quantization_config fixes "static" activation scales; this variant
+ * is for callers without a calibrated a2 (the same per-tensor scheme, taken
+ * over the current batch).
+ *   All other arguments as moe_w4a8_forward.
+ *   ws: moe_w4a8_dynamic_workspace_size(T, H, I, E, k) bytes (it adds the
+ *       fp32 intermediate [T*k, I]).
+ */
+int moe_w4a8_forward_dynamic(const uint8_t* x_e4m3, const float* a1_scale, int T, int H, int I, int E, int k,
+                             const int32_t* w_gu, const float* s_gu, const int32_t* w_d, const float* s_d,
+                             float* a2_out, int act, const int32_t* topk_ids, const float* topk_w,
+                             const int32_t* counts, const int32_t* offsets, const int32_t* sorted_ids,
+                             const int32_t* inv_perm, uint16_t* out_bf16, void* ws, size_t ws_bytes, void* stream);
+size_t moe_w4a8_dynamic_workspace_size(int T, int H, int I, int E, int k);
+
+/*
  * moe_w4a8_forward_static -- moe_w4a8_forward for callers that cannot
  * allocate device memory. The pages have no counterpart: this is a deployment
  * variant of the same computation.

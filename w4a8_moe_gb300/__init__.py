@@ -20,6 +20,7 @@ __all__ = [
     "fp8_block_linear", "w4a8_device_error", "w4a8_set_profile_events", "moe_w4a8_workspace_size",
     "moe_route_workspace_size", "fp8_block_linear_workspace_size", "moe_route_gate",
     "moe_route_gate_workspace_size", "fp8_linear", "fp8_linear_workspace_size",
+    "moe_w4a8_forward_dynamic", "moe_w4a8_dynamic_workspace_size",
     "w4a8_quantize_act_workspace_size", "RouteResult", "library_path", "W4A8Error",
 ]
 
@@ -60,6 +61,9 @@ def _load():
         "moe_w4a8_forward": (i32, [P, P, i32, i32, i32, i32, i32, P, P, P, P, P, i32, P, P, P, P, P,
                                    P, P, P, sz, P]),
         "moe_w4a8_workspace_size": (sz, [i32, i32, i32, i32, i32]),
+        "moe_w4a8_forward_dynamic": (i32, [P, P, i32, i32, i32, i32, i32, P, P, P, P, P, i32, P, P, P, P, P,
+                                           P, P, P, sz, P]),
+        "moe_w4a8_dynamic_workspace_size": (sz, [i32, i32, i32, i32, i32]),
         "fp8_block_linear": (i32, [P, i32, i32, i32, P, P, P, P, P, P, sz, P]),
         "fp8_block_linear_workspace_size": (sz, [i32, i32, i32]),
         "fp8_linear": (i32, [P, P, i32, i32, i32, P, P, P, P, sz, P]),
@@ -104,6 +108,10 @@ def _ws(nbytes: int, device, ws=None):
 # --------------------------------------------------------------------------- sizes
 def moe_w4a8_workspace_size(T, H, I, E, k) -> int:
     return int(_load().moe_w4a8_workspace_size(T, H, I, E, k))
+
+
+def moe_w4a8_dynamic_workspace_size(T, H, I, E, k) -> int:
+    return int(_load().moe_w4a8_dynamic_workspace_size(T, H, I, E, k))
 
 
 def moe_route_workspace_size(T, E, k) -> int:
@@ -215,6 +223,27 @@ def moe_w4a8_forward(x_e4m3, a1_scale, w_gu, s_gu, w_d, s_d, a2_scale, act: int,
         _ptr(route.offsets), _ptr(route.sorted_ids), _ptr(route.inv_perm), _ptr(out), _ptr(ws),
         ws.numel(), _stream(stream)))
     return out
+
+
+def moe_w4a8_forward_dynamic(x_e4m3, a1_scale, w_gu, s_gu, w_d, s_d, act: int, route: RouteResult,
+                             out=None, a2_out=None, ws=None, stream=None):
+    """moe_w4a8_forward with the intermediate scale computed from this call's h:
+    returns (bf16 out [T, H], fp32 a2 [1])."""
+    x = _u8(x_e4m3)
+    T, H = x.shape
+    E, I2, _ = w_gu.shape
+    I = I2 // 2
+    k = route.topk_ids.shape[1]
+    dev = x.device
+    out = out if out is not None else torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    a2_out = a2_out if a2_out is not None else torch.empty(1, dtype=torch.float32, device=dev)
+    ws = _ws(moe_w4a8_dynamic_workspace_size(T, H, I, E, k), dev, ws)
+    _check(_load().moe_w4a8_forward_dynamic(
+        _ptr(x), _ptr(a1_scale), T, H, I, E, k, _ptr(w_gu), _ptr(s_gu), _ptr(w_d), _ptr(s_d),
+        _ptr(a2_out), int(act), _ptr(route.topk_ids), _ptr(route.topk_w), _ptr(route.counts),
+        _ptr(route.offsets), _ptr(route.sorted_ids), _ptr(route.inv_perm), _ptr(out), _ptr(ws),
+        ws.numel(), _stream(stream)))
+    return out, a2_out
 
 
 def fp8_linear(x_e4m3, x_scale, w_e4m3, w_scale, out=None, ws=None, stream=None):

@@ -141,8 +141,10 @@ struct MoeWs {
     uint8_t* hq;
     unsigned long long* s0h;
     float* ypart;
+    float* hf;             // dynamic intermediate scale only
+    unsigned int* hmax;    // header word at byte 64 (dynamic only)
 };
-static size_t moe_ws(int T, int H, int I, int k, MoeWs* w, void* ws)
+static size_t moe_ws(int T, int H, int I, int k, MoeWs* w, void* ws, bool dynamic = false)
 {
     Carver c(ws);
     const size_t A = static_cast<size_t>(T) * k;
@@ -151,6 +153,8 @@ static size_t moe_ws(int T, int H, int I, int k, MoeWs* w, void* ws)
     w->hq = c.take<uint8_t>(A * I);
     w->s0h = c.take<unsigned long long>(A * 8);
     w->ypart = c.take<float>(static_cast<size_t>(moe_ksplit_max(T, k)) * A * H * 4);
+    w->hf = c.take<float>(dynamic ? A * I * 4 : 0);
+    w->hmax = ws ? reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + 64) : nullptr;
     return c.off;
 }
 
@@ -344,11 +348,16 @@ size_t moe_w4a8_workspace_size(int T, int H, int I, int E, int k)
     return moe_ws(T, H, I, k, &w, nullptr);
 }
 
-int moe_w4a8_forward(const uint8_t* x_e4m3, const float* a1_scale, int T, int H, int I, int E, int k,
-                     const int32_t* w_gu, const float* s_gu, const int32_t* w_d, const float* s_d,
-                     const float* a2_scale, int act, const int32_t* topk_ids, const float* topk_w,
-                     const int32_t* counts, const int32_t* offsets, const int32_t* sorted_ids,
-                     const int32_t* inv_perm, uint16_t* out_bf16, void* ws, size_t ws_bytes, void* stream)
+}  // extern "C"
+
+// The MoE forward with a static (a2_scale read) or dynamic (computed from the
+// call's h and written to a2_out) intermediate scale.
+static int moe_forward_common(const uint8_t* x_e4m3, const float* a1_scale, int T, int H, int I, int E, int k,
+                              const int32_t* w_gu, const float* s_gu, const int32_t* w_d, const float* s_d,
+                              const float* a2_scale, float* a2_out, bool dynamic, int act,
+                              const int32_t* topk_ids, const float* topk_w, const int32_t* counts,
+                              const int32_t* offsets, const int32_t* sorted_ids, const int32_t* inv_perm,
+                              uint16_t* out_bf16, void* ws, size_t ws_bytes, void* stream)
 {
     const void* ptrs[] = {x_e4m3, a1_scale, w_gu, s_gu, w_d, s_d, a2_scale, topk_ids, topk_w,
                           counts, offsets, sorted_ids, inv_perm, out_bf16};
@@ -362,7 +371,8 @@ int moe_w4a8_forward(const uint8_t* x_e4m3, const float* a1_scale, int T, int H,
     for (const void* p : ptrs)
         if (!aligned16(p))
             return W4A8_ERR_ALIGN;
-    if (!ws || ws_bytes < moe_w4a8_workspace_size(T, H, I, E, k))
+    if (!ws || ws_bytes < (dynamic ? moe_w4a8_dynamic_workspace_size(T, H, I, E, k)
+                                  : moe_w4a8_workspace_size(T, H, I, E, k)))
         return W4A8_ERR_WORKSPACE;
     if (!aligned16(ws))
         return W4A8_ERR_ALIGN;
@@ -370,7 +380,7 @@ int moe_w4a8_forward(const uint8_t* x_e4m3, const float* a1_scale, int T, int H,
     if (int st = current_device(&sms))
         return st;
     MoeWs w;
-    moe_ws(T, H, I, k, &w, ws);
+    moe_ws(T, H, I, k, &w, ws, dynamic);
     MoeLaunch L{};
     L.xq = x_e4m3;
     L.a1 = a1_scale;
@@ -397,11 +407,46 @@ int moe_w4a8_forward(const uint8_t* x_e4m3, const float* a1_scale, int T, int H,
     L.hq = w.hq;
     L.s0h = w.s0h;
     L.ypart = w.ypart;
+    L.dynamic = dynamic ? 1 : 0;
+    L.hf = w.hf;
+    L.hmax = w.hmax;
+    L.a2_out = a2_out;
     L.err = static_cast<uint32_t*>(ws);
     for (int i = 0; i < 4; ++i)
         L.events[i] = g_profile_events[i];
     const MoeConfig cfg = moe_pick_config(T, H, I, E, k, sms);
     return launch_moe_forward(L, cfg, sms, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" {
+
+int moe_w4a8_forward(const uint8_t* x_e4m3, const float* a1_scale, int T, int H, int I, int E, int k,
+                     const int32_t* w_gu, const float* s_gu, const int32_t* w_d, const float* s_d,
+                     const float* a2_scale, int act, const int32_t* topk_ids, const float* topk_w,
+                     const int32_t* counts, const int32_t* offsets, const int32_t* sorted_ids,
+                     const int32_t* inv_perm, uint16_t* out_bf16, void* ws, size_t ws_bytes, void* stream)
+{
+    return moe_forward_common(x_e4m3, a1_scale, T, H, I, E, k, w_gu, s_gu, w_d, s_d, a2_scale, nullptr, false,
+                              act, topk_ids, topk_w, counts, offsets, sorted_ids, inv_perm, out_bf16, ws, ws_bytes,
+                              stream);
+}
+
+size_t moe_w4a8_dynamic_workspace_size(int T, int H, int I, int E, int k)
+{
+    (void)E;
+    MoeWs w;
+    return moe_ws(T, H, I, k, &w, nullptr, true);
+}
+
+int moe_w4a8_forward_dynamic(const uint8_t* x_e4m3, const float* a1_scale, int T, int H, int I, int E, int k,
+                             const int32_t* w_gu, const float* s_gu, const int32_t* w_d, const float* s_d,
+                             float* a2_out, int act, const int32_t* topk_ids, const float* topk_w,
+                             const int32_t* counts, const int32_t* offsets, const int32_t* sorted_ids,
+                             const int32_t* inv_perm, uint16_t* out_bf16, void* ws, size_t ws_bytes, void* stream)
+{
+    return moe_forward_common(x_e4m3, a1_scale, T, H, I, E, k, w_gu, s_gu, w_d, s_d, a2_out, a2_out, true, act,
+                              topk_ids, topk_w, counts, offsets, sorted_ids, inv_perm, out_bf16, ws, ws_bytes,
+                              stream);
 }
 
 size_t fp8_block_linear_workspace_size(int M, int N, int K)

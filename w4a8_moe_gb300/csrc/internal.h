@@ -76,6 +76,9 @@ struct MoeLaunch {
     uint16_t* out;
     // workspace pieces
     uint8_t* xp; long long* s0x; uint8_t* hq; unsigned long long* s0h; float* ypart;
+    // dynamic intermediate scale (moe_w4a8_forward_dynamic): h in fp32, its
+    // max as float bits, the scale written to a2_out
+    int dynamic; float* hf; unsigned int* hmax; float* a2_out;
     uint32_t* err;
     void* events[4];  // optional cudaEvent_t recorded around the GEMMs
 };

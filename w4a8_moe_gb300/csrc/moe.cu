@@ -55,6 +55,11 @@ struct MoeGemmParams {
     unsigned long long* s0h; // [A] sum_i 512*dec(hq), accumulated by atomics
     // down epilogue
     float* ypart;            // [ksplit or nslots, A, H] raw accumulator (before shift removal)
+    // gate_up with a dynamic intermediate scale: h goes to hf (fp32, natural
+    // column order) and max|h| to *hmax (float bits) instead of hq / s0h
+    int dynamic;
+    float* hf;               // [A, I]
+    unsigned int* hmax;
     int streamk;             // down only: equal stage ranges per CTA (see WorkIter)
     int nslots;              // stream-K: partial slots per output (unused ones zeroed)
     uint32_t* err;
@@ -619,6 +624,7 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                     load_acc(ch * 32, v);
                     const float my_shift = static_cast<float>(my_s0x) * (1.0f / 64.0f);
                     int s512[16];
+                    float hmax_l = 0.0f;
 #pragma unroll
                     for (int cc = 0; cc < 16; ++cc) {
                         // gate lanes finish column cc, up lanes column 16+cc
@@ -634,10 +640,23 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                             const float G = fmaf(512.0f, pg, -shift);
                             const float U = fmaf(512.0f, pu, -shift);
                             const float h = act_fn(sg * G, p.act) * (su * U);
-                            const uint32_t code = cvt_e4m3(h * inv_a2);
-                            p.hq[static_cast<int64_t>(pos) * p.I + kperm(i)] = static_cast<uint8_t>(code);
-                            s512[cc] = e4m3_times512(code);
+                            if (p.dynamic) {
+                                p.hf[static_cast<int64_t>(pos) * p.I + i] = h;
+                                hmax_l = fmaxf(hmax_l, fabsf(h));
+                            } else {
+                                const uint32_t code = cvt_e4m3(h * inv_a2);
+                                p.hq[static_cast<int64_t>(pos) * p.I + kperm(i)] = static_cast<uint8_t>(code);
+                                s512[cc] = e4m3_times512(code);
+                            }
                         }
+                    }
+                    if (p.dynamic) {
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1)
+                            hmax_l = fmaxf(hmax_l, __shfl_xor_sync(0xFFFFFFFFu, hmax_l, o));
+                        if (lane == 0 && hmax_l > 0.0f)   // non-negative floats order like their bits
+                            atomicMax(p.hmax, __float_as_uint(hmax_l));
+                        continue;
                     }
                     // reduce-scatter over the 16 lanes of each half: lane ends
                     // with the sum of column ch*32 + lane over this warp's rows
@@ -708,13 +727,16 @@ __global__ void __launch_bounds__(128) moe_gather_kernel(const uint8_t* __restri
                                                          const int32_t* __restrict__ sorted_ids,
                                                          int A, uint8_t* __restrict__ xp,
                                                          long long* __restrict__ s0x,
-                                                         unsigned long long* __restrict__ s0h)
+                                                         unsigned long long* __restrict__ s0h,
+                                                         unsigned int* __restrict__ hmax)
 {
     // one block per assignment row: every 16-byte chunk of the row is in
     // flight at once
     __shared__ long long red[4];
     grid_dep_wait();
     grid_dep_launch();
+    if (hmax && blockIdx.x == 0 && threadIdx.x == 0)
+        *hmax = 0u;   // max|h| of the dynamic intermediate scale starts at zero
     const int pos = blockIdx.x;
     const int t = __ldg(sorted_ids + pos) / k;
     const uint4* src = reinterpret_cast<const uint4*>(xq + static_cast<int64_t>(t) * H);
@@ -745,6 +767,59 @@ __global__ void __launch_bounds__(128) moe_gather_kernel(const uint8_t* __restri
             total += red[w];
         s0x[pos] = total;
         s0h[pos] = 0ull;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Dynamic intermediate scale: a2 = max|h| / 448 over every assignment of the
+// call (1 if all h are zero), then hq = E4M3(h / a2) in the permuted K order
+// of unpack8 and the exact row sums s0h[pos] = sum_i 512*dec(hq). One block per
+// assignment row; 8 consecutive h per thread.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) moe_hquant_kernel(const float* __restrict__ hf, int I,
+                                                         const unsigned int* __restrict__ hmax,
+                                                         float* __restrict__ a2_out,
+                                                         uint8_t* __restrict__ hq,
+                                                         unsigned long long* __restrict__ s0h)
+{
+    grid_dep_wait();
+    grid_dep_launch();
+    __shared__ long long red[8];
+    const float mx = __uint_as_float(__ldcg(hmax));
+    const float s2 = (mx > 0.0f && mx <= 3.4028234663852886e38f) ? __fdiv_rn(mx, 448.0f) : 1.0f;
+    const float inv = 1.0f / s2;
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        *a2_out = s2;
+    const int pos = blockIdx.x;
+    const float4* row = reinterpret_cast<const float4*>(hf + static_cast<int64_t>(pos) * I);
+    uint2* dst = reinterpret_cast<uint2*>(hq + static_cast<int64_t>(pos) * I);
+    long long sum = 0;
+    for (int g = threadIdx.x; g < I / 8; g += blockDim.x) {
+        const float4 a = __ldcg(row + 2 * g), b = __ldcg(row + 2 * g + 1);
+        const float h[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        uint32_t c[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            c[j] = cvt_e4m3(h[j] * inv);
+            sum += e4m3_times512(c[j]);
+        }
+        // byte order inside the group: elements 0,2,4,6 then 1,3,5,7
+        uint2 o;
+        o.x = c[0] | (c[2] << 8) | (c[4] << 16) | (c[6] << 24);
+        o.y = c[1] | (c[3] << 8) | (c[5] << 16) | (c[7] << 24);
+        dst[g] = o;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+    if ((threadIdx.x & 31) == 0)
+        red[threadIdx.x >> 5] = sum;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        long long t = 0;
+        for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w)
+            t += red[w];
+        s0h[pos] = static_cast<unsigned long long>(t);
     }
 }
 
@@ -917,7 +992,7 @@ int launch_moe_forward(const MoeLaunch& L, const MoeConfig& cfg, int num_sms, cu
     const int BN = cfg.bn, KC = cfg.kc;
     // activations: gather + exact per-token sums
     if (launch_dependent(moe_gather_kernel, dim3(A), dim3(128), 0, s, L.xq, L.H, L.k, L.sorted_ids, A, L.xp,
-                         L.s0x, L.s0h) != cudaSuccess)
+                         L.s0x, L.s0h, L.dynamic ? L.hmax : nullptr) != cudaSuccess)
         return kErrLaunch;
 
     // weight boxes: 64-byte rows (64-byte swizzle) for KC = 128, else 128-byte rows
@@ -959,6 +1034,9 @@ int launch_moe_forward(const MoeLaunch& L, const MoeConfig& cfg, int num_sms, cu
     // gate_up: 64 gated pairs (128 weight rows) per tile, full K = H
     mark(0);
     MoeGemmParams gu = g;
+    gu.dynamic = L.dynamic;
+    gu.hf = L.hf;
+    gu.hmax = L.hmax;
     gu.rows_per_expert = 2 * L.I;
     gu.rt_count = L.I / 64;
     gu.kblocks = L.H / KC;
@@ -968,6 +1046,10 @@ int launch_moe_forward(const MoeLaunch& L, const MoeConfig& cfg, int num_sms, cu
     int st = dispatch_gemm<0>(cfg, tw_gu, tb_gu, gu, grid, s);
     if (st != kOK)
         return st;
+    if (L.dynamic &&
+        launch_dependent(moe_hquant_kernel, dim3(A), dim3(256), 0, s, static_cast<const float*>(L.hf), L.I,
+                         static_cast<const unsigned int*>(L.hmax), L.a2_out, L.hq, L.s0h) != cudaSuccess)
+        return kErrLaunch;
     mark(1);
 
     // down: 128 output rows per tile, K = I split ksplit ways
@@ -993,7 +1075,8 @@ int launch_moe_forward(const MoeLaunch& L, const MoeConfig& cfg, int num_sms, cu
              : parts <= 8 ? moe_finalize_kernel<8> : moe_finalize_kernel<kMaxKsplit>;
     if (launch_dependent(fin, dim3(static_cast<unsigned>((nthreads + 255) / 256)), dim3(256), 0, s,
                          L.T, L.H, L.k, A, parts, L.ids, L.topk_w, L.inv, L.ypart,
-                         static_cast<const unsigned long long*>(L.s0h), L.s_d, L.a2, L.out) != cudaSuccess)
+                         static_cast<const unsigned long long*>(L.s0h), L.s_d,
+                         L.dynamic ? static_cast<const float*>(L.a2_out) : L.a2, L.out) != cudaSuccess)
         return kErrLaunch;
     mark(3);
     return kOK;
