@@ -55,8 +55,8 @@ struct MoeGemmParams {
     unsigned long long* s0h; // [A] sum_i 512*dec(hq), accumulated by atomics
     // down epilogue
     float* ypart;            // [ksplit or nslots, A, H] raw accumulator (before shift removal)
-    // gate_up with a dynamic intermediate scale: h goes to hf (fp32, natural
-    // column order) and max|h| to *hmax (float bits) instead of hq / s0h
+    // gate_up with a dynamic intermediate scale (MODE 2): h goes to hf (fp32,
+    // natural column order) and max|h| to *hmax (float bits) instead of hq / s0h
     int dynamic;
     float* hf;               // [A, I]
     unsigned int* hmax;
@@ -92,6 +92,17 @@ struct MoeTraits {
     static constexpr int kPar = NCONV / 4;                       // converter warps per quadrant
     static_assert(kWBytes % 1024 == 0 && kXBytes % 1024 == 0 && kASlot % 1024 == 0, "stage alignment");
     static_assert(NXT >= 0 && NXT <= NX, "TMEM A slots");
+    // where X slot x keeps its unpacked A; a compile-time constant unless the
+    // slots are mixed (a runtime test in the hot loops costs real time)
+    __device__ __forceinline__ static bool a_in_tmem(int x)
+    {
+        if constexpr (NXT == NX)
+            return true;
+        else if constexpr (NXT == 0)
+            return false;
+        else
+            return x < NXT;
+    }
     static_assert(kSmem <= 232448, "shared memory budget");
     static_assert(kTmemNeed <= 512, "tensor memory budget");
     static_assert(BN % 16 == 0 && BN <= 256, "token tile");
@@ -130,7 +141,7 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const int* s_cnt, const i
     const int c = s_cnt[e];
     const int ntt = (c + BN - 1) / BN;
     ti.e = e;
-    if (MODE == 0) {
+    if (MODE != 1) {   // gate_up (static or dynamic scale)
         const int per_rt = ntt * ksplit;
         ti.rt = local / per_rt;
         const int r2 = local - ti.rt * per_rt;
@@ -377,7 +388,7 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                             // one box = 128 rows x kWBoxBytes (gate_up: 64 gate + 64 up rows)
                             uint8_t* wd = st + wa * 128 * Tr::kWBoxBytes;
                             const int kx = kel / 2 + wa * Tr::kWBoxBytes;
-                            if (MODE == 0) {
+                            if (MODE != 1) {   // gate_up (static or dynamic scale)
                                 const int r0 = ti.e * p.rows_per_expert + ti.rt * 64;
                                 tma_load_2d_hint(smem_u32(wd), &tm_w, kx, r0, fb, pol);
                                 tma_load_2d_hint(smem_u32(wd + 64 * Tr::kWBoxBytes), &tm_w, kx, r0 + p.I, fb, pol);
@@ -445,7 +456,7 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                         tc_fence_after();
                         const uint8_t* st = xring + x * Tr::kXBytes;
                         const uint64_t bd0 = desc_kmajor_sw128(smem_u32(st));
-                        const bool a_tmem = x < NXT;
+                        const bool a_tmem = Tr::a_in_tmem(x);
                         const uint64_t ad0 =
                             a_tmem ? 0 : desc_kmajor_sw128(smem_u32(aring + (x - NXT) * Tr::kASlot));
 #pragma unroll
@@ -488,7 +499,7 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
         const int par = (warp - 4) >> 2;
         const int r = 32 * q + lane;  // A row == TMEM lane
         int src = r;
-        if (MODE == 0) {
+        if (MODE != 1) {   // gate_up (static or dynamic scale)
             // lanes 0-15 of each quadrant: gate rows; lanes 16-31: the matching
             // up rows (so one warp holds both halves of a gated pair)
             src = (lane < 16) ? (16 * q + lane) : (64 + 16 * q + (lane - 16));
@@ -525,7 +536,7 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                             unpack8(w4.z, o[8 * c4 + 4], o[8 * c4 + 5]);
                             unpack8(w4.w, o[8 * c4 + 6], o[8 * c4 + 7]);
                         }
-                        if (x < NXT) {
+                        if (Tr::a_in_tmem(x)) {
                             tmem_st32(tmem_a + (static_cast<uint32_t>(q * 32) << 16) +
                                           static_cast<uint32_t>(x * Tr::kACols + half * 32),
                                       o);
@@ -541,7 +552,7 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                     __syncwarp();
                     if (lane == 0)
                         mbar_arrive(smem_u32(&wfree[w]));
-                    if (x < NXT) {
+                    if (Tr::a_in_tmem(x)) {
                         tmem_st_wait();
                         tc_fence_before();
                     } else {
@@ -609,7 +620,7 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                 tmem_ld_wait();
             };
             const int nchunks = (ti.ntok + 31) >> 5;
-            if (MODE == 0) {
+            if (MODE != 1) {   // gate_up (static or dynamic scale)
                 const int half = lane >> 4;  // 0: gate lane, 1: up lane
                 const int i = ti.rt * 64 + 16 * q + (lane & 15);
                 const float sg = a1 * __ldg(p.s_gu + static_cast<int64_t>(ti.e) * 2 * p.I + i);
@@ -640,7 +651,7 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                             const float G = fmaf(512.0f, pg, -shift);
                             const float U = fmaf(512.0f, pu, -shift);
                             const float h = act_fn(sg * G, p.act) * (su * U);
-                            if (p.dynamic) {
+                            if (MODE == 2) {
                                 p.hf[static_cast<int64_t>(pos) * p.I + i] = h;
                                 hmax_l = fmaxf(hmax_l, fabsf(h));
                             } else {
@@ -650,7 +661,7 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                             }
                         }
                     }
-                    if (p.dynamic) {
+                    if (MODE == 2) {
 #pragma unroll
                         for (int o = 16; o > 0; o >>= 1)
                             hmax_l = fmaxf(hmax_l, __shfl_xor_sync(0xFFFFFFFFu, hmax_l, o));
@@ -1043,7 +1054,8 @@ int launch_moe_forward(const MoeLaunch& L, const MoeConfig& cfg, int num_sms, cu
     gu.ksplit = 1;
     int64_t tiles = static_cast<int64_t>(gu.rt_count) * tok_tiles_max;
     int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
-    int st = dispatch_gemm<0>(cfg, tw_gu, tb_gu, gu, grid, s);
+    int st = L.dynamic ? dispatch_gemm<2>(cfg, tw_gu, tb_gu, gu, grid, s)
+                       : dispatch_gemm<0>(cfg, tw_gu, tb_gu, gu, grid, s);
     if (st != kOK)
         return st;
     if (L.dynamic &&
