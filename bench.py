@@ -93,9 +93,9 @@ def max_over_ranks(x: float, world: int) -> float:
 NCU_TRAFFIC = {
     "sources": ["w4a8_moe_gb300/csrc/moe.cu", "w4a8_moe_gb300/csrc/ptx.cuh",
                 "w4a8_moe_gb300/csrc/internal.h"],
-    "sha256": "5317ff6adc7bc811515948b2f29aee0b2182ee062074ee1a3b5f81f971169a91",
-    "gate_up": 470996736 + 4179200,
-    "down": 235840512 + 4016128,
+    "sha256": "31f87cee8c16d6f7541a5ff3b9b26f1569b3031124a07cfce4e2526ae5c15161",
+    "gate_up": 471007744 + 4014592,
+    "down": 235878144 + 4146688,
 }
 
 
