@@ -91,7 +91,7 @@ def max_over_ranks(x: float, world: int) -> float:
 # Mixtral decode layer (profiles/moe_gemm_mixtral_decode.md), valid only for
 # the GEMM sources they were taken on: a changed kernel reports null.
 NCU_TRAFFIC = {
-    "sources": ["w4a8_moe_gb300/csrc/moe.cu", "w4a8_moe_gb300/csrc/ptx.cuh",
+    "sources": ["w4a8_moe_gb300/csrc/moe.cu", "w4a8_moe_gb300/csrc/ptx.cuh", "w4a8_moe_gb300/csrc/sched.cuh",
                 "w4a8_moe_gb300/csrc/internal.h"],
     "sha256": "31f87cee8c16d6f7541a5ff3b9b26f1569b3031124a07cfce4e2526ae5c15161",
     "gate_up": 471007744 + 4014592,

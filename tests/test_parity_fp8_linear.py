@@ -56,7 +56,8 @@ def test_fp8_linear_prefill_sampled_rows(N, K):
 
 
 @pytest.mark.parametrize("M,N,K", [(5, 256, 384), (37, 384, 256), (100, 128, 1024),
-                                   (200, 256, 512), (300, 384, 384), (17, 1024, 2048)])
+                                   (200, 256, 512), (300, 384, 384), (17, 1024, 2048),
+                                   (10, 2048, 4096)])   # stream-K, ~10 segments per tile
 def test_fp8_linear_ragged(M, N, K):
     lib, xq, sx, wq, sw = _case(M, N, K, seed=M + N)
     y = lib.fp8_linear(xq, sx, wq, sw)
