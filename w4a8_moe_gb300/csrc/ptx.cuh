@@ -88,7 +88,9 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity
 // stream has completed and its writes are visible (a no-op when the kernel was
 // not launched as a dependent), and allow the next kernel to start launching.
 // Every kernel of this library calls grid_dep_launch only after its own
-// grid_dep_wait has returned.
+// grid_dep_wait has returned, except the block-FP8 activation quantizer, whose
+// only dependent (the block-FP8 GEMM) reads nothing but the weights before its
+// own wait.
 __device__ __forceinline__ void grid_dep_wait()
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");

@@ -206,9 +206,14 @@ __global__ void __launch_bounds__(256) block_act_quant_kernel(const uint16_t* __
                                                               float* __restrict__ xs_t, int ld_t,
                                                               int* __restrict__ zero, int nzero)
 {
-    // the workspace may still be in use by the previous call's GEMM
-    grid_dep_wait();
+    // The one dependent of this kernel is the block-FP8 GEMM of the same call,
+    // which before its own wait only streams the weights (written by no kernel
+    // of this library), so it may launch at once: its weight stream then
+    // overlaps this kernel and the previous call's tail. This kernel itself
+    // waits before touching the workspace, which the previous call's GEMM may
+    // still be using.
     grid_dep_launch();
+    grid_dep_wait();
     // clear the GEMM's split-K tile counters of this call
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nzero;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x)
