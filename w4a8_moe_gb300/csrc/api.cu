@@ -306,7 +306,8 @@ int moe_route_gate(const uint16_t* hidden_bf16, const uint16_t* gate_bf16, int T
     RouteGateWs w;
     route_gate_ws(T, H, E, k, &w, ws);
     float* logits = logits_out ? logits_out : w.logits;
-    return launch_route_gate(hidden_bf16, gate_bf16, T, H, E, k, renormalize ? 1 : 0, logits, topk_ids, topk_w,
+    return launch_route_gate(hidden_bf16, gate_bf16, T, H, E, k, renormalize ? 1 : 0, logits, logits_out ? 1 : 0,
+                             topk_ids, topk_w,
                              counts, offsets, sorted_ids, inv_perm, w.partial, w.done, w.hist, w.base,
                              static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? W4A8_OK

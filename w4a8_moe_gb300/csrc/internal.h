@@ -51,7 +51,7 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, i
                          int32_t* inv, int32_t* block_hist, int32_t* block_base, cudaStream_t s);
 int route_gate_slice(int T, int H, int E, int k);
 cudaError_t launch_route_gate(const uint16_t* x, const uint16_t* gate, int T, int H, int E, int k,
-                              int renorm, float* logits, int32_t* ids, float* w, int32_t* counts,
+                              int renorm, float* logits, int write_logits, int32_t* ids, float* w, int32_t* counts,
                               int32_t* offsets, int32_t* sorted_ids, int32_t* inv, float* partial,
                               int* done, int32_t* block_hist, int32_t* block_base, cudaStream_t s);
 

@@ -314,7 +314,8 @@ __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v 
 // and builds the permutation. `done` is zero at entry and left zero.
 __global__ void __launch_bounds__(512) route_gate_fused_kernel(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ gate, int T, int H, int E, int k,
-    int renorm, int HS, float* __restrict__ partial, float* __restrict__ logits, int32_t* __restrict__ ids,
+    int renorm, int HS, float* __restrict__ partial, float* __restrict__ logits, int write_logits,
+    int32_t* __restrict__ ids,
     float* __restrict__ w, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
     int32_t* __restrict__ sorted_ids, int32_t* __restrict__ inv, int* __restrict__ done)
 {
@@ -394,15 +395,20 @@ __global__ void __launch_bounds__(512) route_gate_fused_kernel(
     for (int i = threadIdx.x; i < S * TE; i += blockDim.x)
         red[i] = __ldcg(partial + i);
     __syncthreads();
+    // the logits stay in shared memory for the routing (and go to global
+    // memory only when the caller asked for them)
+    float* lg = red + kRouteGatePartials;
     for (int i = threadIdx.x; i < TE; i += blockDim.x) {
         float acc = 0.0f;
         for (int q = 0; q < S; ++q)
             acc += red[q * TE + i];
-        logits[i] = acc;
+        lg[i] = acc;
+        if (write_logits)
+            logits[i] = acc;
     }
     __syncthreads();
     for (int t = wid; t < T; t += 16)
-        route_token<true>(logits, t, E, k, renorm, ids, w, s_ids);
+        route_token<true>(lg, t, E, k, renorm, ids, w, s_ids);
     route_block_tail(s_ids, T * k, E, counts, offsets, sorted_ids, inv, cnt, base, wcnt);
     if (threadIdx.x == 0)
         *done = 0;
@@ -489,20 +495,22 @@ int route_gate_slice(int T, int H, int E, int k)
 }
 
 cudaError_t launch_route_gate(const uint16_t* x, const uint16_t* gate, int T, int H, int E, int k,
-                              int renorm, float* logits, int32_t* ids, float* w, int32_t* counts,
+                              int renorm, float* logits, int write_logits, int32_t* ids, float* w, int32_t* counts,
                               int32_t* offsets, int32_t* sorted_ids, int32_t* inv, float* partial,
                               int* done, int32_t* block_hist, int32_t* block_base, cudaStream_t s)
 {
     const int A = T * k;
     const int hs = route_gate_slice(T, H, E, k);
     if (hs) {
-        const size_t dyn = static_cast<size_t>(kRouteGatePartials) * 4;
+        // partial logits, then the summed logits [T, E] (T*E <= the partials' count)
+        const size_t dyn = static_cast<size_t>(kRouteGatePartials) * 4 * 2;
         cudaError_t e = cudaFuncSetAttribute(route_gate_fused_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(dyn));
         if (e != cudaSuccess)
             return e;
         return launch_dependent(route_gate_fused_kernel, dim3(H / hs), dim3(512), dyn, s, x, gate, T, H, E, k,
-                                renorm, hs, partial, logits, ids, w, counts, offsets, sorted_ids, inv, done);
+                                renorm, hs, partial, logits, write_logits, ids, w, counts, offsets, sorted_ids,
+                                inv, done);
     }
     const int nb = (A + kRouteChunk - 1) / kRouteChunk;
     cudaError_t e = launch_dependent(route_gate_topk_kernel, dim3((T + 7) / 8), dim3(256), 0, s, x, gate, T, H,
