@@ -591,7 +591,7 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                             const float G = fmaf(512.0f, pg, -shift);
                             const float U = fmaf(512.0f, pu, -shift);
                             const float h = act_fn(sg * G, p.act) * (su * U);
-                            if (MODE == 2) {
+                            if constexpr (MODE == 2) {
                                 p.hf[static_cast<int64_t>(pos) * p.I + i] = h;
                                 hmax_l = fmaxf(hmax_l, fabsf(h));
                             } else {
@@ -601,30 +601,30 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                             }
                         }
                     }
-                    if (MODE == 2) {
+                    if constexpr (MODE == 2) {
 #pragma unroll
                         for (int o = 16; o > 0; o >>= 1)
                             hmax_l = fmaxf(hmax_l, __shfl_xor_sync(0xFFFFFFFFu, hmax_l, o));
                         if (lane == 0 && hmax_l > 0.0f)   // non-negative floats order like their bits
                             atomicMax(p.hmax, __float_as_uint(hmax_l));
-                        continue;
-                    }
-                    // reduce-scatter over the 16 lanes of each half: lane ends
-                    // with the sum of column ch*32 + lane over this warp's rows
+                    } else {
+                        // reduce-scatter over the 16 lanes of each half: lane ends
+                        // with the sum of column ch*32 + lane over this warp's rows
 #pragma unroll
-                    for (int m = 8; m >= 1; m >>= 1) {
-                        const bool upper = (lane & m) != 0;
+                        for (int m = 8; m >= 1; m >>= 1) {
+                            const bool upper = (lane & m) != 0;
 #pragma unroll
-                        for (int x = 0; x < m; ++x) {
-                            const int send = upper ? s512[x] : s512[x + m];
-                            const int recv = __shfl_xor_sync(0xFFFFFFFFu, send, m);
-                            s512[x] = (upper ? s512[x + m] : s512[x]) + recv;
+                            for (int x = 0; x < m; ++x) {
+                                const int send = upper ? s512[x] : s512[x + m];
+                                const int recv = __shfl_xor_sync(0xFFFFFFFFu, send, m);
+                                s512[x] = (upper ? s512[x + m] : s512[x]) + recv;
+                            }
                         }
+                        const int col = ch * 32 + lane;
+                        if (col < ti.ntok && s512[0] != 0)
+                            atomicAdd(p.s0h + ti.tok0 + col,
+                                      static_cast<unsigned long long>(static_cast<long long>(s512[0])));
                     }
-                    const int col = ch * 32 + lane;
-                    if (col < ti.ntok && s512[0] != 0)
-                        atomicAdd(p.s0h + ti.tok0 + col,
-                                  static_cast<unsigned long long>(static_cast<long long>(s512[0])));
                 }
             } else {
                 const int n = ti.rt * 128 + q * 32 + lane;

@@ -50,6 +50,9 @@ MOE_SHAPES = {
                                32768, 8, 2, 1, 0.0),
     "grok_prefill": MoEShape("Grok-1 MoE layer prefill T32768 H6144 I32768 E8 k2 GELU-tanh skewed",
                              32768, 6144, 32768, 8, 2, 1, 1.0),
+    # a prefill-shaped layer small enough for detailed profiling (a few GB on the device)
+    "grok_prefill_8k": MoEShape("Grok-1 MoE layer prefill T8192 H6144 I32768 E8 k2 GELU-tanh skewed",
+                                8192, 6144, 32768, 8, 2, 1, 1.0),
 }
 
 BLOCK_FP8_SHAPES = [(16384, 2560), (13312, 2560), (2560, 6144)]
