@@ -93,9 +93,9 @@ def max_over_ranks(x: float, world: int) -> float:
 NCU_TRAFFIC = {
     "sources": ["w4a8_moe_gb300/csrc/moe.cu", "w4a8_moe_gb300/csrc/ptx.cuh", "w4a8_moe_gb300/csrc/sched.cuh",
                 "w4a8_moe_gb300/csrc/internal.h"],
-    "sha256": "31f87cee8c16d6f7541a5ff3b9b26f1569b3031124a07cfce4e2526ae5c15161",
-    "gate_up": 471007744 + 4014592,
-    "down": 235878144 + 4146688,
+    "sha256": "51ffc627ef35c3b24d67313a826bcf4b0332ad18dcf4754722182af7ede2ee16",
+    "gate_up": 471007744 + 3898112,
+    "down": 235854592 + 4094976,
 }
 
 
