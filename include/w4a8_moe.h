@@ -284,6 +284,17 @@ size_t fp8_block_linear_workspace_size(int M, int N, int K);
 int w4a8_set_profile_events(void* const* events, int count);
 
 /*
+ * w4a8_selftest_wait_timeout -- test hook for the error path of the pipelined
+ * kernels (the pages have no counterpart). Every mbarrier wait of those kernels
+ * gives up after a cycle budget and sets the workspace error word, which
+ * w4a8_device_error reports as W4A8_ERR_TIMEOUT. This call runs one small
+ * kernel that waits on a barrier nothing completes, with a budget of about
+ * 10 ms, so that error is recorded in ws (at least 256 bytes, 16-byte aligned)
+ * without any other effect; the context stays usable.
+ */
+int w4a8_selftest_wait_timeout(void* ws, void* stream);
+
+/*
  * w4a8_device_error -- read and clear the device error word of a workspace.
  * Synchronizes `stream` (the only call that does). *code_out receives
  * W4A8_OK, or W4A8_ERR_TIMEOUT when a kernel gave up on a bounded wait since

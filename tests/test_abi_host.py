@@ -103,6 +103,16 @@ def test_route_gate_validation_before_the_device(lib):
         assert call() == 5                                              # no sm_103 device, no fallback
 
 
+def test_selftest_hook_validates_its_workspace(lib):
+    f = lib.w4a8_selftest_wait_timeout
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    assert f(None, None) == 1                     # NULL
+    assert f(_vp(0x10004), None) == 3             # alignment
+    if not torch.cuda.is_available():
+        assert f(_vp(0x10000), None) == 5         # no sm_103 device
+
+
 def test_forward_shape_rules(lib):
     P, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
     f = lib.moe_w4a8_forward

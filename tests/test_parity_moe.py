@@ -38,6 +38,7 @@ def test_tiny_layer_all_tokens():
     (300, 256, 256, 8, 2, 0),     # 256-token tiles, several per expert
     (7, 256, 256, 1, 1, 0),       # E = 1, k = 1: dense W4A8 MLP
     (64, 768, 512, 16, 4, 1),     # k = 4, 16 experts, H not a power of two
+    (64, 256, 256, 256, 8, 0),    # the most experts the boundary accepts, top-8
 ])
 def test_shapes_and_tails(T, H, I, E, k, act):
     case = MoECase(T, H, I, E, k, act, seed=T + E)

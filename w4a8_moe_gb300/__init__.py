@@ -17,7 +17,7 @@ import torch
 
 __all__ = [
     "w4a8_quantize_experts", "w4a8_quantize_act", "moe_route", "moe_w4a8_forward",
-    "fp8_block_linear", "w4a8_device_error", "w4a8_set_profile_events", "moe_w4a8_workspace_size",
+    "fp8_block_linear", "w4a8_device_error", "w4a8_selftest_wait_timeout", "w4a8_set_profile_events", "moe_w4a8_workspace_size",
     "moe_route_workspace_size", "fp8_block_linear_workspace_size", "moe_route_gate",
     "moe_route_gate_workspace_size", "fp8_linear", "fp8_linear_workspace_size",
     "moe_w4a8_forward_dynamic", "moe_w4a8_dynamic_workspace_size",
@@ -69,6 +69,7 @@ def _load():
         "fp8_linear": (i32, [P, P, i32, i32, i32, P, P, P, P, sz, P]),
         "fp8_linear_workspace_size": (sz, [i32, i32, i32]),
         "w4a8_device_error": (i32, [P, P, P]),
+        "w4a8_selftest_wait_timeout": (i32, [P, P]),
         "w4a8_set_profile_events": (i32, [P, i32]),
     }
     for name, (res, args) in sig.items():
@@ -288,6 +289,11 @@ def w4a8_set_profile_events(events) -> None:
             e.record()
     arr = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
     _check(_load().w4a8_set_profile_events(arr, len(events)))
+
+
+def w4a8_selftest_wait_timeout(ws, stream=None):
+    """Record a wait timeout in ws from a kernel whose barrier never completes (test hook)."""
+    _check(_load().w4a8_selftest_wait_timeout(_ptr(ws), _stream(stream)))
 
 
 def w4a8_device_error(ws, stream=None) -> int:

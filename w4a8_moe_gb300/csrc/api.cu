@@ -551,6 +551,20 @@ int w4a8_set_profile_events(void* const* events, int count)
     return W4A8_OK;
 }
 
+int w4a8_selftest_wait_timeout(void* ws, void* stream)
+{
+    if (!ws)
+        return W4A8_ERR_NULL;
+    if (!aligned16(ws))
+        return W4A8_ERR_ALIGN;
+    int sms;
+    if (int st = current_device(&sms))
+        return st;
+    return launch_selftest_wait_timeout(static_cast<uint32_t*>(ws), static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? W4A8_OK
+               : W4A8_ERR_LAUNCH;
+}
+
 int w4a8_device_error(void* ws, int* code_out, void* stream)
 {
     if (!ws || !code_out)

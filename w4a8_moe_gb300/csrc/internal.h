@@ -113,6 +113,9 @@ struct FpLaunch {
 };
 int launch_fp8_linear(const FpLaunch& L, const FpConfig& cfg, int num_sms, cudaStream_t s);
 
+// ---- selftest.cu
+cudaError_t launch_selftest_wait_timeout(uint32_t* err, cudaStream_t s);
+
 // ---- api.cu (tensor-map encoding through the driver entry point)
 bool encode_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
                    uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows,

@@ -50,8 +50,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 // Bounded wait for the phase with the given parity to complete. Returns false
-// when the budget runs out (the caller records the error and unwinds).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+// when the budget (clock64 cycles) runs out: the caller records the error and
+// unwinds.
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, long long budget)
 {
     if (mbar_try_wait(bar, parity))
         return true;
@@ -59,10 +60,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
     for (uint32_t it = 0; it < kWaitMaxPolls; ++it) {
         if (mbar_try_wait(bar, parity))
             return true;
-        if (clock64() - t0 > kWaitBudgetCycles)
+        if (clock64() - t0 > budget)
             break;
     }
     return false;
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+{
+    return mbar_wait_for(bar, parity, kWaitBudgetCycles);
 }
 
 // Same, but also gives up as soon as another role of the CTA has set *abort
