@@ -26,10 +26,11 @@
  *    other device, or without a device, calls return W4A8_ERR_DEVICE. There is
  *    no CPU fallback.
  *  - Workspace: calls that take `ws` need ws_bytes >= the matching
- *    *_workspace_size(). The first 256 bytes of every workspace hold a device
- *    error word; the caller zero-fills a workspace once when it allocates it.
- *    Kernels only OR bits into that word (a bounded wait that ran out sets
- *    bit 0); w4a8_device_error() reads and clears it.
+ *    *_workspace_size(). The first 256 bytes of every workspace are a header:
+ *    the caller zero-fills them once when it allocates the workspace. Byte 0
+ *    holds a device error word that kernels only OR bits into (a bounded wait
+ *    that ran out sets bit 0); w4a8_device_error() reads and clears it. Calls
+ *    may keep other counters in the header; every call leaves them zero.
  *  - Stateless and thread-safe; concurrent calls must use distinct workspaces.
  */
 #ifndef W4A8_MOE_H
@@ -172,6 +173,28 @@ int moe_w4a8_forward(const uint8_t* x_e4m3, const float* a1_scale, int T, int H,
                      const int32_t* sorted_ids, const int32_t* inv_perm, uint16_t* out_bf16,
                      void* ws, size_t ws_bytes, void* stream);
 size_t moe_w4a8_workspace_size(int T, int H, int I, int E, int k);
+
+/*
+ * moe_w4a8_plan -- the launch plan moe_w4a8_forward (dynamic = 0) or
+ * moe_w4a8_forward_dynamic (dynamic = 1) uses for a shape on a GPU with
+ * num_sms SMs. Host only: no device is touched, so it also runs without a
+ * GPU. The plan does not change the result beyond the order in which fp32
+ * partial sums of the down projection are added.
+ *
+ *   plan [8] int32 (host), out:
+ *     [0] token tile (MMA N bound: 32, 64, 128 or 256)
+ *     [1] K elements per pipeline stage
+ *     [2] K split of the down projection
+ *     [3] 1 when the down projection runs stream-K (equal K ranges per CTA)
+ *     [4] stream-K partial slots per output (0 otherwise)
+ *     [5] 1 when both projections run in one launch (static scale, token tile
+ *         up to 128), 0 when gate_up and down are separate launches
+ *     [6] kernel launches of one forward call
+ *     [7] partial sums per output that the combine adds
+ *   Returns W4A8_ERR_SHAPE for shapes moe_w4a8_forward rejects or
+ *   num_sms < 1, W4A8_ERR_NULL for a null plan.
+ */
+int moe_w4a8_plan(int T, int H, int I, int E, int k, int dynamic, int num_sms, int32_t* plan);
 
 /*
  * moe_w4a8_forward_dynamic -- moe_w4a8_forward with the intermediate

@@ -149,3 +149,55 @@ def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(pkg, "_LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(pkg.W4A8Error):
         pkg.moe_route_workspace_size(4, 8, 2)
+
+
+def _plan(lib, T, H, I, E, k, dynamic=0, sms=152):
+    f = lib.moe_w4a8_plan
+    f.argtypes = [ctypes.c_int] * 7 + [ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    out = (ctypes.c_int32 * 8)()
+    st = f(T, H, I, E, k, dynamic, sms, ctypes.cast(out, ctypes.c_void_p))
+    return st, list(out)
+
+
+def test_plan_of_the_decode_and_prefill_layers(lib):
+    """The host planner (no GPU needed): decode-sized layers with the static
+    scale run both projections in one launch, the dynamic scale and the
+    256-token tiles of a prefill run them separately."""
+    st, p = _plan(lib, 32, 4096, 14336, 8, 2)                  # Mixtral decode
+    assert st == 0 and p[0] == 32 and p[5] == 1 and p[6] == 3
+    assert (14336 // p[1]) % p[2] == 0 and p[7] == p[2] and p[3] == 0
+    st, p = _plan(lib, 32, 4096, 14336, 8, 2, dynamic=1)
+    assert st == 0 and p[5] == 0 and p[6] == 5                  # + the scale's quantizer
+    st, p = _plan(lib, 1, 6144, 32768, 8, 2)                   # Grok single token
+    assert st == 0 and p[5] == 1 and p[2] > 1                   # the down K is split to fill the SMs
+    st, p = _plan(lib, 32768, 6144, 32768, 8, 2)               # Grok prefill
+    assert st == 0 and p[0] == 256 and p[5] == 0 and p[6] == 4 and p[7] == 1
+
+
+def test_plan_rejects_what_the_forward_rejects(lib):
+    assert _plan(lib, 32, 4096 + 128, 14336, 8, 2)[0] == 2
+    assert _plan(lib, 0, 4096, 14336, 8, 2)[0] == 2
+    assert _plan(lib, 32, 4096, 14336, 8, 2, sms=0)[0] == 2
+    f = lib.moe_w4a8_plan
+    f.argtypes = [ctypes.c_int] * 7 + [ctypes.c_void_p]
+    assert f(32, 4096, 14336, 8, 2, 0, 152, None) == 1
+
+
+def test_plan_fits_the_workspace(lib):
+    """Whatever split the planner picks, its fp32 partial sums fit the
+    workspace the size query promises, and every K split divides the K blocks
+    into at least two stages (the two MMA issuers)."""
+    lib.moe_w4a8_workspace_size.restype = ctypes.c_size_t
+    for T in (1, 2, 3, 5, 8, 16, 31, 32, 33, 64, 100, 128, 129, 300, 1024):
+        for (H, I, E, k) in ((4096, 14336, 8, 2), (6144, 32768, 8, 2), (256, 512, 16, 4), (2048, 1536, 64, 6),
+                             (512, 256, 256, 8)):
+            for dyn in (0, 1):
+                for sms in (152, 148, 7):
+                    st, p = _plan(lib, T, H, I, E, k, dyn, sms)
+                    assert st == 0
+                    kb = I // p[1]
+                    assert kb % p[2] == 0 and kb // p[2] >= 2 or p[2] == 1
+                    ws = lib.moe_w4a8_workspace_size(T, H, I, E, k)
+                    assert ws >= p[7] * T * k * H * 4, (T, H, I, E, k, dyn, sms, p)
+                    assert p[5] in (0, 1) and (p[5] == 0 or (dyn == 0 and p[0] <= 128))

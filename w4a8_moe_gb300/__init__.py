@@ -61,6 +61,7 @@ def _load():
         "moe_w4a8_forward": (i32, [P, P, i32, i32, i32, i32, i32, P, P, P, P, P, i32, P, P, P, P, P,
                                    P, P, P, sz, P]),
         "moe_w4a8_workspace_size": (sz, [i32, i32, i32, i32, i32]),
+        "moe_w4a8_plan": (i32, [i32, i32, i32, i32, i32, i32, i32, P]),
         "moe_w4a8_forward_dynamic": (i32, [P, P, i32, i32, i32, i32, i32, P, P, P, P, P, i32, P, P, P, P, P,
                                            P, P, P, sz, P]),
         "moe_w4a8_dynamic_workspace_size": (sz, [i32, i32, i32, i32, i32]),
@@ -109,6 +110,21 @@ def _ws(nbytes: int, device, ws=None):
 # --------------------------------------------------------------------------- sizes
 def moe_w4a8_workspace_size(T, H, I, E, k) -> int:
     return int(_load().moe_w4a8_workspace_size(T, H, I, E, k))
+
+
+_PLAN_KEYS = ("token_tile", "k_per_stage", "down_ksplit", "down_streamk", "down_slots", "one_launch",
+              "launches", "partials")
+
+
+def moe_w4a8_plan(T, H, I, E, k, dynamic=False, num_sms=None) -> dict:
+    """The launch plan of the MoE forward for this shape (host only; see
+    moe_w4a8_plan in include/w4a8_moe.h). num_sms defaults to the current
+    device's SM count."""
+    if num_sms is None:
+        num_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    plan = (ctypes.c_int32 * 8)()
+    _check(_load().moe_w4a8_plan(T, H, I, E, k, 1 if dynamic else 0, num_sms, plan))
+    return dict(zip(_PLAN_KEYS, list(plan)))
 
 
 def moe_w4a8_dynamic_workspace_size(T, H, I, E, k) -> int:

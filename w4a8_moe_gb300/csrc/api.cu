@@ -143,6 +143,7 @@ struct MoeWs {
     float* ypart;
     float* hf;             // dynamic intermediate scale only
     unsigned int* hmax;    // header word at byte 64 (dynamic only)
+    int* done;             // [256] per-expert progress counters (one-launch forward)
 };
 static size_t moe_ws(int T, int H, int I, int k, MoeWs* w, void* ws, bool dynamic = false)
 {
@@ -154,8 +155,17 @@ static size_t moe_ws(int T, int H, int I, int k, MoeWs* w, void* ws, bool dynami
     w->s0h = c.take<unsigned long long>(A * 8);
     w->ypart = c.take<float>(static_cast<size_t>(moe_ksplit_max(T, k)) * A * H * 4);
     w->hf = c.take<float>(dynamic ? A * I * 4 : 0);
+    w->done = c.take<int>(256 * 4);
     w->hmax = ws ? reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + 64) : nullptr;
     return c.off;
+}
+
+// Shapes the MoE forward accepts (see the header).
+static bool moe_shape_ok(int T, int H, int I, int E, int k)
+{
+    return T >= 1 && H >= 256 && H % 256 == 0 && I >= 256 && I % 256 == 0 && E >= 1 && E <= 256 && k >= 1 &&
+           k <= E && static_cast<int64_t>(T) * k < (static_cast<int64_t>(1) << 30) &&
+           static_cast<int64_t>(E) * 2 * I < (static_cast<int64_t>(1) << 31);
 }
 
 struct BlkWs {
@@ -349,6 +359,26 @@ size_t moe_w4a8_workspace_size(int T, int H, int I, int E, int k)
     return moe_ws(T, H, I, k, &w, nullptr);
 }
 
+int moe_w4a8_plan(int T, int H, int I, int E, int k, int dynamic, int num_sms, int32_t* plan)
+{
+    if (!plan)
+        return W4A8_ERR_NULL;
+    if (!moe_shape_ok(T, H, I, E, k) || num_sms < 1)
+        return W4A8_ERR_SHAPE;
+    const MoeConfig c = moe_pick_config(T, H, I, E, k, num_sms, dynamic == 0);
+    const bool one = c.fused && dynamic == 0;
+    plan[0] = c.bn;
+    plan[1] = c.kc;
+    plan[2] = c.ksplit;
+    plan[3] = one ? 0 : c.streamk;
+    plan[4] = one ? 0 : c.nslots;
+    plan[5] = one ? 1 : 0;
+    // gather, the GEMM launch(es), the dynamic scale's quantizer, the combine
+    plan[6] = 1 + (one ? 1 : 2) + (dynamic ? 1 : 0) + 1;
+    plan[7] = (one || !c.streamk) ? c.ksplit : c.nslots;
+    return W4A8_OK;
+}
+
 }  // extern "C"
 
 // The MoE forward with a static (a2_scale read) or dynamic (computed from the
@@ -365,9 +395,7 @@ static int moe_forward_common(const uint8_t* x_e4m3, const float* a1_scale, int 
     for (const void* p : ptrs)
         if (!p)
             return W4A8_ERR_NULL;
-    if (T < 1 || H < 256 || H % 256 != 0 || I < 256 || I % 256 != 0 || E < 1 || E > 256 || k < 1 ||
-        k > E || (act != 0 && act != 1) || static_cast<int64_t>(T) * k >= (static_cast<int64_t>(1) << 30) ||
-        static_cast<int64_t>(E) * 2 * I >= (static_cast<int64_t>(1) << 31))
+    if (!moe_shape_ok(T, H, I, E, k) || (act != 0 && act != 1))
         return W4A8_ERR_SHAPE;
     for (const void* p : ptrs)
         if (!aligned16(p))
@@ -408,6 +436,10 @@ static int moe_forward_common(const uint8_t* x_e4m3, const float* a1_scale, int 
     L.hq = w.hq;
     L.s0h = w.s0h;
     L.ypart = w.ypart;
+    L.done = w.done;
+    // header words 48 and 49: the one-launch forward's claim counters, zero
+    // when the workspace is allocated and left zero by every call
+    L.claim = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + 192);
     L.dynamic = dynamic ? 1 : 0;
     L.hf = w.hf;
     L.hmax = w.hmax;
@@ -415,7 +447,7 @@ static int moe_forward_common(const uint8_t* x_e4m3, const float* a1_scale, int 
     L.err = static_cast<uint32_t*>(ws);
     for (int i = 0; i < 4; ++i)
         L.events[i] = g_profile_events[i];
-    const MoeConfig cfg = moe_pick_config(T, H, I, E, k, sms);
+    const MoeConfig cfg = moe_pick_config(T, H, I, E, k, sms, !dynamic);
     return launch_moe_forward(L, cfg, sms, static_cast<cudaStream_t>(stream));
 }
 

@@ -64,8 +64,11 @@ struct MoeConfig {
     int ksplit;    // split of the down projection's K (round-robin tiles)
     int streamk;   // 1: the down GEMM takes equal K-block ranges per CTA
     int nslots;    // stream-K partial slots per output
+    int fused;     // 1: gate_up and down run in one launch (K split ksplit ways)
 };
-MoeConfig moe_pick_config(int T, int H, int I, int E, int k, int num_sms);
+// one_launch: whether the caller's path allows both projections in one
+// launch (not with the dynamic intermediate scale, which needs max|h| first)
+MoeConfig moe_pick_config(int T, int H, int I, int E, int k, int num_sms, bool one_launch);
 int moe_ksplit_max(int T, int k);
 struct MoeLaunch {
     const uint8_t* xq; const float* a1; int T, H, I, E, k;
@@ -76,6 +79,8 @@ struct MoeLaunch {
     uint16_t* out;
     // workspace pieces
     uint8_t* xp; long long* s0x; uint8_t* hq; unsigned long long* s0h; float* ypart;
+    int* done;  // [E] per-expert gate_up progress of the one-launch forward
+    int* claim; // [2] its tile-claim counters (zero between calls)
     // dynamic intermediate scale (moe_w4a8_forward_dynamic): h in fp32, its
     // max as float bits, the scale written to a2_out
     int dynamic; float* hf; unsigned int* hmax; float* a2_out;

@@ -63,6 +63,11 @@ struct MoeGemmParams {
     unsigned int* hmax;
     int streamk;             // down only: equal stage ranges per CTA (see WorkIter)
     int nslots;              // stream-K: partial slots per output (unused ones zeroed)
+    // MODE 3 runs both projections in one launch: the fields above
+    // (rows_per_expert .. ksplit) describe its gate_up tiles, these its down tiles
+    int rows_per_expert2, rt_count2, kblocks2, ksplit2;
+    int* done;               // [E] gate_up tiles finished per expert, x4 (one per epilogue warp)
+    int* claim;              // [2] MODE 3: tiles claimed, CTAs finished (both zero between launches)
     uint32_t* err;
 };
 
@@ -79,8 +84,10 @@ struct MoeTraits {
     // X slots 0..NXT-1 keep their unpacked A in TMEM, slots NXT..NX-1 in
     // shared memory (after the B tiles)
     static constexpr int kData = NW * kWBytes + NX * kXBytes + (NX - NXT) * kASlot;
-    static constexpr int kBars = 2 * NW + 3 * NX + 4 + 2;        // + drain barriers
-    static constexpr int kCtrl = kBars * 8 + 16 + 4 * (256 + 260 + 260);
+    static constexpr int kBars = 2 * NW + 3 * NX + 4 + 2 + 2 * kTileQ;   // + drain, tile queue
+    static constexpr int kCtrl = kBars * 8 + 16 + 4 * (256 + 260 + 260 + 260 + kTileQ);
+    // MODE 3 tile queue: every role but the weight producer frees each entry
+    static constexpr int kTileReaders = 1 + NISS + NCONV + 4;
     static constexpr int kSmem = 1024 + kData + kCtrl;
     // two accumulator buffers (tile i / tile i+1), each with one partial sum
     // per MMA-issuing thread
@@ -160,6 +167,35 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const int* s_cnt, const i
     return ti;
 }
 
+// MODE 3 (both projections in one launch): the CTA-shared list holds the
+// gate_up tiles [0, n_gu) followed by the down tiles. Every CTA takes its
+// tiles in increasing order, so all of its gate_up tiles come before any of
+// its down tiles; a down tile of expert e waits (once per CTA and expert)
+// until every gate_up tile of e has been written.
+template <int MODE>
+__device__ __forceinline__ bool tile_is_gate_up(int t, int n_gu)
+{
+    if constexpr (MODE == 3)
+        return t < n_gu;
+    else
+        return MODE != 1;
+}
+
+template <int MODE>
+__device__ __forceinline__ TileInfo decode_any(int t, bool gu, const int* s_cnt, const int* s_off, const int* s_pre,
+                                               const int* s_pre2, int n_gu, int BN, const MoeGemmParams& p)
+{
+    if constexpr (MODE == 3) {
+        return gu ? decode_tile<0>(t, s_cnt, s_off, s_pre, p.E, BN, 1, p.rt_count)
+                  : decode_tile<1>(t - n_gu, s_cnt, s_off, s_pre2, p.E, BN, p.ksplit2, p.rt_count2);
+    } else {
+        (void)gu;
+        (void)s_pre2;
+        (void)n_gu;
+        return decode_tile<MODE>(t, s_cnt, s_off, s_pre, p.E, BN, p.ksplit, p.rt_count);
+    }
+}
+
 // Nibbles -> E4M3 operand bytes worth (q + 8) * 2^-9. The two output words
 // hold the weights of one packed word in the order [0,2,4,6 | 1,3,5,7]: the
 // K order inside every group of 8 is permuted, and the activation operands
@@ -207,6 +243,7 @@ __device__ __forceinline__ float act_fn(float z, int act)
 template <int MODE, int BN, int KC, int NW, int NX, int NXT, int NCONV, int NISS>
 __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b,
+                    const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_b2,
                     const MoeGemmParams p)
 {
     using Tr = MoeTraits<MODE, BN, KC, NW, NX, NXT, NCONV, NISS>;
@@ -225,11 +262,15 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
     uint64_t* accfull = xfree + NX;
     uint64_t* accempty = accfull + 2;
     uint64_t* drain = accempty + 2;                 // one per MMA issuer
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain + 2);
+    uint64_t* tq_full = drain + 2;                  // MODE 3 tile queue
+    uint64_t* tq_free = tq_full + kTileQ;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(tq_free + kTileQ);
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
     int* s_cnt = reinterpret_cast<int*>(s_tmem + 4);
     int* s_off = s_cnt + 256;
     int* s_pre = s_off + 260;
+    int* s_pre2 = s_pre + 260;   // MODE 3: the down tiles' prefix over experts
+    volatile int* s_tq = s_pre2 + 260;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -250,12 +291,20 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
         }
         mbar_init(smem_u32(&drain[0]), 1);
         mbar_init(smem_u32(&drain[1]), 1);
+        for (int i = 0; i < kTileQ; ++i) {
+            mbar_init(smem_u32(&tq_full[i]), 1);
+            mbar_init(smem_u32(&tq_free[i]), Tr::kTileReaders);
+        }
         fence_mbar_init();
         *s_abort = 0;
     }
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tm_w);
         prefetch_tmap(&tm_b);
+        if constexpr (MODE == 3) {
+            prefetch_tmap(&tm_w2);
+            prefetch_tmap(&tm_b2);
+        }
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(s_tmem), Tr::kTmemCols);
@@ -269,26 +318,44 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
     // kernel writes) starts at once; only the activation producer and the
     // epilogue, which read or overwrite the predecessor's buffers, wait.
     if (threadIdx.x == 64) {
-        int acc = 0;
+        int acc = 0, acc2 = 0;
         for (int e = 0; e < p.E; ++e) {
             const int c = p.counts[e];
             s_cnt[e] = c;
             s_off[e] = p.offsets[e];
             s_pre[e] = acc;
             acc += p.rt_count * ((c + BN - 1) / BN) * p.ksplit;
+            if constexpr (MODE == 3) {
+                s_pre2[e] = acc2;
+                acc2 += p.rt_count2 * ((c + BN - 1) / BN) * p.ksplit2;
+            }
         }
         s_pre[p.E] = acc;
+        s_pre2[p.E] = acc2;
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
     const uint32_t tmem_a = tmem + Tr::kDCols;   // A of X slots 0..NXT-1
-    const int total = s_pre[p.E];
+    const int n_gu = s_pre[p.E];                   // MODE 3: the gate_up tiles come first
+    const int total = n_gu + (MODE == 3 ? s_pre2[p.E] : 0);
+    const int kb_second = (MODE == 3) ? p.kblocks2 : 0;
 
     auto fail = [&]() {
         *s_abort = 1;
         set_error(p.err, kErrBitTimeout);
+    };
+    // role: 0 the weight producer, 1 another single-thread role, 2 a whole warp.
+    // MODE 3 claims the last kClaimRounds rounds of tiles (and the remainder).
+    constexpr int kClaimRounds = 2;
+    const int n_static = max(0, total / static_cast<int>(gridDim.x) - kClaimRounds) * static_cast<int>(gridDim.x);
+    auto start_seq = [&](TileSeq& sq, int role) {
+        if constexpr (MODE == 3)
+            sq.init_dynamic(role, p.claim, s_tq, smem_u32(tq_full), smem_u32(tq_free), s_abort, total, n_gu,
+                            p.kblocks, kb_second, n_static);
+        else
+            sq.init_static(total, p.kblocks, p.streamk != 0, n_gu, kb_second);
     };
 
     if (warp == 0 || warp == 2) {
@@ -309,17 +376,38 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
             uint32_t issued = 0;       // bit s: slot s was filled at least once
             uint32_t last_par = 0;     // bit s: parity of the last fill of slot s
             bool ok = true;
-            WorkIter wi;
-            for (wi.init(total, p.kblocks, p.streamk != 0); wi.valid() && ok; wi.next()) {
+            int seen = -1;   // MODE 3: experts up to this one have all their gate_up tiles written
+            TileSeq wi;
+            for (start_seq(wi, wprod ? 0 : 1); wi.valid() && ok;) {
                 const int t = wi.t;
-                const TileInfo ti = decode_tile<MODE>(t, s_cnt, s_off, s_pre, p.E, BN, p.ksplit, p.rt_count);
+                const bool gu = tile_is_gate_up<MODE>(t, n_gu);
+                const TileInfo ti = decode_any<MODE>(t, gu, s_cnt, s_off, s_pre, s_pre2, n_gu, BN, p);
+                const bool second = (MODE == 3 && !gu);
+                const int kbl = second ? p.kblocks2 : p.kblocks;
+                const int rpe = second ? p.rows_per_expert2 : p.rows_per_expert;
+                const CUtensorMap* mw = second ? &tm_w2 : &tm_w;
+                const CUtensorMap* mb = second ? &tm_b2 : &tm_b;
+                if constexpr (MODE == 3) {
+                    // the down tile reads the intermediate of expert e (TMA): wait
+                    // until the 4 epilogue warps of each of e's gate_up tiles counted
+                    if (!wprod && second && ti.e > seen) {
+                        const int need = 4 * (s_pre[ti.e + 1] - s_pre[ti.e]);
+                        if (!counter_wait_or_abort(p.done + ti.e, need, s_abort)) {
+                            ok = false;
+                            break;
+                        }
+                        seen = ti.e;
+                    }
+                }
                 for (int kb = wi.kb0; kb < wi.kb0 + wi.nkb; ++kb) {
+                    if (wi.claim_here(kb, 4))
+                        wi.claim_next();
                     if (!mbar_wait_or_abort(smem_u32(&freeb[s]), ph ^ 1u, s_abort)) {
                         ok = false;
                         break;
                     }
                     const uint32_t fb = smem_u32(&fullb[s]);
-                    const int kel = (ti.ks * p.kblocks + kb) * KC;  // first K element
+                    const int kel = (ti.ks * kbl + kb) * KC;  // first K element
                     if (wprod) {
                         mbar_arrive_expect_tx(fb, Tr::kWBytes);
                         uint8_t* st = wring + s * Tr::kWBytes;
@@ -328,13 +416,13 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                             // one box = 128 rows x kWBoxBytes (gate_up: 64 gate + 64 up rows)
                             uint8_t* wd = st + wa * 128 * Tr::kWBoxBytes;
                             const int kx = kel / 2 + wa * Tr::kWBoxBytes;
-                            if (MODE != 1) {   // gate_up (static or dynamic scale)
-                                const int r0 = ti.e * p.rows_per_expert + ti.rt * 64;
-                                tma_load_2d_hint(smem_u32(wd), &tm_w, kx, r0, fb, pol);
-                                tma_load_2d_hint(smem_u32(wd + 64 * Tr::kWBoxBytes), &tm_w, kx, r0 + p.I, fb, pol);
+                            if (gu) {   // gate_up (static or dynamic scale)
+                                const int r0 = ti.e * rpe + ti.rt * 64;
+                                tma_load_2d_hint(smem_u32(wd), mw, kx, r0, fb, pol);
+                                tma_load_2d_hint(smem_u32(wd + 64 * Tr::kWBoxBytes), mw, kx, r0 + p.I, fb, pol);
                             } else {
-                                const int r0 = ti.e * p.rows_per_expert + ti.rt * 128;
-                                tma_load_2d_hint(smem_u32(wd), &tm_w, kx, r0, fb, pol);
+                                const int r0 = ti.e * rpe + ti.rt * 128;
+                                tma_load_2d_hint(smem_u32(wd), mw, kx, r0, fb, pol);
                             }
                         }
                     } else {
@@ -342,7 +430,7 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                         uint8_t* st = xring + s * Tr::kXBytes;
 #pragma unroll
                         for (int a = 0; a < Tr::kAtoms; ++a)
-                            tma_load_2d_hint(smem_u32(st + a * BN * 128), &tm_b, kel + a * 128, ti.tok0, fb, pol);
+                            tma_load_2d_hint(smem_u32(st + a * BN * 128), mb, kel + a * 128, ti.tok0, fb, pol);
                     }
                     issued |= 1u << s;
                     last_par = (last_par & ~(1u << s)) | (ph << s);
@@ -351,7 +439,10 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                         ph ^= 1u;
                     }
                 }
+                if (ok)   // (after a failed wait nothing more is published)
+                    wi.next();
             }
+            ok = ok && wi.ok;
             if (!ok) {
                 fail();
                 // let every issued copy land before the CTA's shared memory goes away
@@ -373,9 +464,10 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
             uint32_t g = 0;
             int it = 0;
             bool ok = true;
-            WorkIter wi;
-            for (wi.init(total, p.kblocks, p.streamk != 0); wi.valid() && ok; wi.next(), ++it) {
-                const TileInfo ti = decode_tile<MODE>(wi.t, s_cnt, s_off, s_pre, p.E, BN, p.ksplit, p.rt_count);
+            TileSeq wi;
+            for (start_seq(wi, 1); wi.valid() && ok; wi.next(), ++it) {
+                const TileInfo ti = decode_any<MODE>(wi.t, tile_is_gate_up<MODE>(wi.t, n_gu), s_cnt, s_off, s_pre,
+                                                     s_pre2, n_gu, BN, p);
                 const int nmma = max(16, (ti.ntok + 15) & ~15);
                 const uint32_t idesc = idesc_e4m3_f32(128, nmma);
                 const int d = it & 1;
@@ -425,6 +517,7 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                     break;
                 umma_commit(smem_u32(&accfull[d]));   // (an issuer with no stage in this tile arrives at once)
             }
+            ok = ok && wi.ok;
             if (!ok) {
                 fail();
                 umma_commit(smem_u32(&drain[me]));  // wait for MMAs in flight before TMEM goes away
@@ -438,18 +531,16 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
         const int q = warp & 3;
         const int par = (warp - 4) >> 2;
         const int r = 32 * q + lane;  // A row == TMEM lane
-        int src = r;
-        if (MODE != 1) {   // gate_up (static or dynamic scale)
-            // lanes 0-15 of each quadrant: gate rows; lanes 16-31: the matching
-            // up rows (so one warp holds both halves of a gated pair)
-            src = (lane < 16) ? (16 * q + lane) : (64 + 16 * q + (lane - 16));
-        }
+        // gate_up: lanes 0-15 of each quadrant take gate rows, lanes 16-31 the
+        // matching up rows (so one warp holds both halves of a gated pair)
+        const int src_gu = (lane < 16) ? (16 * q + lane) : (64 + 16 * q + (lane - 16));
         int w = 0, x = 0;
         uint32_t wph = 0, xph = 0;
         uint32_t g = 0;
         bool ok = true;
-        WorkIter wi;
-        for (wi.init(total, p.kblocks, p.streamk != 0); wi.valid() && ok; wi.next()) {
+        TileSeq wi;
+        for (start_seq(wi, 2); wi.valid() && ok; wi.next()) {
+            const int src = tile_is_gate_up<MODE>(wi.t, n_gu) ? src_gu : r;
             for (int kb = 0; kb < wi.nkb; ++kb, ++g) {
                 if (static_cast<int>(g % Tr::kPar) == par) {
                     if (!mbar_wait_or_abort(smem_u32(&wfull[w]), wph, s_abort) ||
@@ -512,6 +603,7 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                 }
             }
         }
+        ok = ok && wi.ok;
         if (!ok)
             fail();
     } else if (warp >= Tr::kEpi0) {
@@ -524,9 +616,10 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
         uint32_t gsum = 0;   // global stage index of the tile's first stage
         int it = 0;
         bool ok = true;
-        WorkIter wi;
-        for (wi.init(total, p.kblocks, p.streamk != 0); wi.valid() && ok; wi.next(), ++it) {
-            const TileInfo ti = decode_tile<MODE>(wi.t, s_cnt, s_off, s_pre, p.E, BN, p.ksplit, p.rt_count);
+        TileSeq wi;
+        for (start_seq(wi, 2); wi.valid() && ok; wi.next(), ++it) {
+            const bool gu = tile_is_gate_up<MODE>(wi.t, n_gu);
+            const TileInfo ti = decode_any<MODE>(wi.t, gu, s_cnt, s_off, s_pre, s_pre2, n_gu, BN, p);
             const int d = it & 1;
             const uint32_t use = static_cast<uint32_t>(it >> 1);
             if (!mbar_wait_or_abort(smem_u32(&accfull[d]), use & 1u, s_abort)) {
@@ -560,7 +653,7 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                 tmem_ld_wait();
             };
             const int nchunks = (ti.ntok + 31) >> 5;
-            if (MODE != 1) {   // gate_up (static or dynamic scale)
+            if (gu) {   // gate_up (static or dynamic scale)
                 const int half = lane >> 4;  // 0: gate lane, 1: up lane
                 const int i = ti.rt * 64 + 16 * q + (lane & 15);
                 const float sg = a1 * __ldg(p.s_gu + static_cast<int64_t>(ti.e) * 2 * p.I + i);
@@ -626,6 +719,18 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                                       static_cast<unsigned long long>(static_cast<long long>(s512[0])));
                     }
                 }
+                if constexpr (MODE == 3) {
+                    // publish this warp's quarter of the tile to the down tiles
+                    // (which read it with TMA, in other CTAs): every lane's
+                    // stores are made visible before lane 0 counts
+                    __threadfence();
+                    fence_proxy_async_global();
+                    __syncwarp();
+                    if (lane == 0) {
+                        __threadfence();
+                        atomicAdd(p.done + ti.e, 1);
+                    }
+                }
             } else {
                 const int n = ti.rt * 128 + q * 32 + lane;
                 int slot = p.streamk ? wi.slot : ti.ks;
@@ -656,12 +761,25 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
             if (lane == 0)
                 mbar_arrive(smem_u32(&accempty[d]));
         }
+        ok = ok && wi.ok;
         if (!ok)
             fail();
     }
 
     tc_fence_before();
     __syncthreads();
+    if constexpr (MODE == 3) {
+        // the last CTA to finish has seen every claim of this launch: leave
+        // the claim counters zero for the next one
+        if (threadIdx.x == 0) {
+            __threadfence();
+            if (atomicAdd(p.claim + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+                atomicExch(p.claim, 0);
+                atomicExch(p.claim + 1, 0);
+                __threadfence();
+            }
+        }
+    }
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
@@ -679,7 +797,8 @@ __global__ void __launch_bounds__(128) moe_gather_kernel(const uint8_t* __restri
                                                          int A, uint8_t* __restrict__ xp,
                                                          long long* __restrict__ s0x,
                                                          unsigned long long* __restrict__ s0h,
-                                                         unsigned int* __restrict__ hmax)
+                                                         unsigned int* __restrict__ hmax, int* __restrict__ done,
+                                                         int E)
 {
     // one block per assignment row: every 16-byte chunk of the row is in
     // flight at once
@@ -688,6 +807,9 @@ __global__ void __launch_bounds__(128) moe_gather_kernel(const uint8_t* __restri
     grid_dep_launch();
     if (hmax && blockIdx.x == 0 && threadIdx.x == 0)
         *hmax = 0u;   // max|h| of the dynamic intermediate scale starts at zero
+    if (done && blockIdx.x == 0)
+        for (int e = threadIdx.x; e < E; e += blockDim.x)
+            done[e] = 0;   // per-expert gate_up progress of the one-launch forward
     const int pos = blockIdx.x;
     const int t = __ldg(sorted_ids + pos) / k;
     const uint4* src = reinterpret_cast<const uint4*>(xq + static_cast<int64_t>(t) * H);
@@ -859,11 +981,63 @@ static int pick_bn(int T)
     return 256;
 }
 
-MoeConfig moe_pick_config(int T, int H, int I, int E, int k, int num_sms)
+// One launch for both projections (static intermediate scale, token tiles
+// up to 128): the CTAs take the gate_up tiles and then the down tiles round
+// robin, so an SM that runs out of gate_up tiles streams down weights at once
+// instead of idling until the slowest gate_up CTA ends. The down split is
+// picked for the balance of that whole list, assuming the T*k assignments
+// spread evenly over min(E, T*k) experts: the cost of a split d is the most
+// stages any CTA gets (plus one per tile, the accumulator hand-off) plus the
+// reduction of the d partial sums, counted in stage times of the whole GPU.
+static int fused_ksplit(int T, int H, int I, int E, int k, int bn, int kc, int num_sms)
+{
+    const int64_t A = static_cast<int64_t>(T) * k;
+    const int64_t act = A < E ? A : E;
+    const int64_t per = (A + act - 1) / act;
+    const int64_t ntt = (per + bn - 1) / bn;
+    const int64_t n_gu = act * (I / 64) * ntt;
+    const int kb_gu = H / kc, kb_all = I / kc;
+    const int kmax = moe_ksplit_max(T, k);
+    const int64_t G = num_sms;
+    const double stage_bytes = static_cast<double>(G) * 128 * kc / 2;   // one stage on every SM
+    int best = 1;
+    double best_cost = 0.0;
+    for (int d = 1; d <= kmax; ++d) {
+        if (kb_all % d != 0 || kb_all / d < 2)
+            continue;
+        const int kb_dn = kb_all / d;
+        const int64_t n = n_gu + act * (H / 128) * ntt * d;
+        int64_t worst = 0;
+        for (int64_t c = 0; c < G && c < n; ++c) {
+            const int64_t mine = (n - c + G - 1) / G;
+            const int64_t mine_gu = c < n_gu ? (n_gu - c + G - 1) / G : 0;
+            const int64_t cost = mine_gu * (kb_gu + 1) + (mine - mine_gu) * (kb_dn + 1);
+            worst = cost > worst ? cost : worst;
+        }
+        // partial sums: written once, read once by the combine
+        const double red = 2.0 * d * static_cast<double>(A) * H * 4 / stage_bytes;
+        const double cost = static_cast<double>(worst) + (d > 1 ? red : 0.0);
+        if (d == 1 || cost < best_cost) {
+            best_cost = cost;
+            best = d;
+        }
+    }
+    return best;
+}
+
+MoeConfig moe_pick_config(int T, int H, int I, int E, int k, int num_sms, bool one_launch)
 {
     MoeConfig c;
     c.bn = pick_bn(T);
     c.kc = (c.bn <= 128) ? 256 : 128;
+    c.fused = 0;
+    if (one_launch && c.kc == 256) {
+        c.fused = 1;
+        c.ksplit = fused_ksplit(T, H, I, E, k, c.bn, c.kc, num_sms);
+        c.streamk = 0;
+        c.nslots = 0;
+        return c;
+    }
     // Split the down projection's K so that its tiles fill the SMs: the cost
     // of a split d is waves(d) * (stages per tile + a fixed per-tile cost of
     // about one stage: the accumulator hand-off and the epilogue tail).
@@ -908,15 +1082,15 @@ MoeConfig moe_pick_config(int T, int H, int I, int E, int k, int num_sms)
 }
 
 template <int MODE, int BN, int KC, int NW, int NX, int NXT, int NCONV, int NISS>
-static int launch_gemm(const CUtensorMap& tw, const CUtensorMap& tb, const MoeGemmParams& prm, int grid,
-                       cudaStream_t s)
+static int launch_gemm(const CUtensorMap& tw, const CUtensorMap& tb, const CUtensorMap& tw2, const CUtensorMap& tb2,
+                       const MoeGemmParams& prm, int grid, cudaStream_t s)
 {
     using Tr = MoeTraits<MODE, BN, KC, NW, NX, NXT, NCONV, NISS>;
     auto kern = moe_gemm_kernel<MODE, BN, KC, NW, NX, NXT, NCONV, NISS>;
     // attribute set on every launch: cheap, and correct for every device
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Tr::kSmem) != cudaSuccess)
         return kErrLaunch;
-    return launch_dependent(kern, dim3(grid), dim3(Tr::kThreads), Tr::kSmem, s, tw, tb, prm) == cudaSuccess
+    return launch_dependent(kern, dim3(grid), dim3(Tr::kThreads), Tr::kSmem, s, tw, tb, tw2, tb2, prm) == cudaSuccess
                ? kOK
                : kErrLaunch;
 }
@@ -925,15 +1099,20 @@ static int launch_gemm(const CUtensorMap& tw, const CUtensorMap& tb, const MoeGe
 // tensor memory, which leaves shared memory to a deep TMA ring (192 KB); the
 // 256-token tile needs all of TMEM for its two accumulators and keeps A in
 // shared memory.
+// MODE 3 (both projections in one launch) exists for the TMEM-A shapes only.
 template <int MODE>
-static int dispatch_gemm(const MoeConfig& cfg, const CUtensorMap& tw, const CUtensorMap& tb,
-                         const MoeGemmParams& prm, int grid, cudaStream_t s)
+static int dispatch_gemm(const MoeConfig& cfg, const CUtensorMap& tw, const CUtensorMap& tb, const CUtensorMap& tw2,
+                         const CUtensorMap& tb2, const MoeGemmParams& prm, int grid, cudaStream_t s)
 {
     switch (cfg.bn) {
-    case 32: return launch_gemm<MODE, 32, 256, 10, 6, 6, 8, 2>(tw, tb, prm, grid, s);
-    case 64: return launch_gemm<MODE, 64, 256, 8, 4, 4, 8, 2>(tw, tb, prm, grid, s);
-    case 128: return launch_gemm<MODE, 128, 256, 4, 4, 4, 8, 1>(tw, tb, prm, grid, s);
-    default: return launch_gemm<MODE, 256, 128, 8, 3, 0, 4, 1>(tw, tb, prm, grid, s);
+    case 32: return launch_gemm<MODE, 32, 256, 10, 6, 6, 8, 2>(tw, tb, tw2, tb2, prm, grid, s);
+    case 64: return launch_gemm<MODE, 64, 256, 8, 4, 4, 8, 2>(tw, tb, tw2, tb2, prm, grid, s);
+    case 128: return launch_gemm<MODE, 128, 256, 4, 4, 4, 8, 1>(tw, tb, tw2, tb2, prm, grid, s);
+    default:
+        if constexpr (MODE == 3)
+            return kErrLaunch;
+        else
+            return launch_gemm<MODE, 256, 128, 8, 3, 0, 4, 1>(tw, tb, tw2, tb2, prm, grid, s);
     }
 }
 
@@ -942,8 +1121,9 @@ int launch_moe_forward(const MoeLaunch& L, const MoeConfig& cfg, int num_sms, cu
     const int A = L.T * L.k;
     const int BN = cfg.bn, KC = cfg.kc;
     // activations: gather + exact per-token sums
+    const bool fused = cfg.fused && !L.dynamic;
     if (launch_dependent(moe_gather_kernel, dim3(A), dim3(128), 0, s, L.xq, L.H, L.k, L.sorted_ids, A, L.xp,
-                         L.s0x, L.s0h, L.dynamic ? L.hmax : nullptr) != cudaSuccess)
+                         L.s0x, L.s0h, L.dynamic ? L.hmax : nullptr, fused ? L.done : nullptr, L.E) != cudaSuccess)
         return kErrLaunch;
 
     // weight boxes: 64-byte rows (64-byte swizzle) for KC = 128, else 128-byte rows
@@ -976,12 +1156,34 @@ int launch_moe_forward(const MoeLaunch& L, const MoeConfig& cfg, int num_sms, cu
     g.hq = L.hq;
     g.s0h = L.s0h;
     g.ypart = L.ypart;
+    g.done = L.done;
+    g.claim = L.claim;
     g.err = L.err;
 
     auto mark = [&](int i) {
         if (L.events[i])
             cudaEventRecord(static_cast<cudaEvent_t>(L.events[i]), s);
     };
+    if (fused) {
+        // one launch: the gate_up tiles, then the down tiles (K split cfg.ksplit ways)
+        MoeGemmParams f = g;
+        f.rows_per_expert = 2 * L.I;
+        f.rt_count = L.I / 64;
+        f.kblocks = L.H / KC;
+        f.ksplit = 1;
+        f.rows_per_expert2 = L.H;
+        f.rt_count2 = L.H / 128;
+        f.ksplit2 = cfg.ksplit;
+        f.kblocks2 = L.I / KC / cfg.ksplit;
+        const int64_t tiles = static_cast<int64_t>(f.rt_count + f.rt_count2 * cfg.ksplit) * tok_tiles_max;
+        const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
+        mark(0);
+        const int st = dispatch_gemm<3>(cfg, tw_gu, tb_gu, tw_d, tb_d, f, grid, s);
+        if (st != kOK)
+            return st;
+        mark(1);
+        mark(2);
+    } else {
     // gate_up: 64 gated pairs (128 weight rows) per tile, full K = H
     mark(0);
     MoeGemmParams gu = g;
@@ -994,8 +1196,8 @@ int launch_moe_forward(const MoeLaunch& L, const MoeConfig& cfg, int num_sms, cu
     gu.ksplit = 1;
     int64_t tiles = static_cast<int64_t>(gu.rt_count) * tok_tiles_max;
     int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
-    int st = L.dynamic ? dispatch_gemm<2>(cfg, tw_gu, tb_gu, gu, grid, s)
-                       : dispatch_gemm<0>(cfg, tw_gu, tb_gu, gu, grid, s);
+    int st = L.dynamic ? dispatch_gemm<2>(cfg, tw_gu, tb_gu, tw_gu, tb_gu, gu, grid, s)
+                       : dispatch_gemm<0>(cfg, tw_gu, tb_gu, tw_gu, tb_gu, gu, grid, s);
     if (st != kOK)
         return st;
     if (L.dynamic &&
@@ -1014,14 +1216,15 @@ int launch_moe_forward(const MoeLaunch& L, const MoeConfig& cfg, int num_sms, cu
     dn.nslots = cfg.nslots;
     tiles = static_cast<int64_t>(dn.rt_count) * tok_tiles_max * dn.ksplit;
     grid = cfg.streamk ? num_sms : static_cast<int>(tiles < num_sms ? tiles : num_sms);
-    st = dispatch_gemm<1>(cfg, tw_d, tb_d, dn, grid, s);
+    st = dispatch_gemm<1>(cfg, tw_d, tb_d, tw_d, tb_d, dn, grid, s);
     if (st != kOK)
         return st;
     mark(2);
+    }
 
     const int64_t nthreads = static_cast<int64_t>(L.T) * (L.H / 4);
     // the register array of split partials is sized for the split in use
-    const int parts = cfg.streamk ? cfg.nslots : cfg.ksplit;
+    const int parts = (cfg.streamk && !fused) ? cfg.nslots : cfg.ksplit;
     auto fin = parts == 1 ? moe_finalize_kernel<1>
              : parts <= 4 ? moe_finalize_kernel<4>
              : parts <= 8 ? moe_finalize_kernel<8> : moe_finalize_kernel<kMaxKsplit>;

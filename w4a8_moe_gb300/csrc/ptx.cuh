@@ -109,6 +109,38 @@ __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+__device__ __forceinline__ int ld_acquire_gpu(const int* p)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Waits until *counter >= target, where other CTAs of the same grid count up
+// after writing data that this thread will then read with TMA: the acquire
+// load orders the reads after those writes, and the proxy fence orders this
+// thread's later async-proxy (TMA) reads after its generic-proxy view. Gives
+// up like mbar_wait_or_abort (budget, or *abort set by another role).
+__device__ __forceinline__ bool counter_wait_or_abort(const int* counter, int target, const volatile int* abort)
+{
+    bool ok = ld_acquire_gpu(counter) >= target;
+    if (!ok) {
+        const long long t0 = clock64();
+        for (uint32_t it = 0; it < kWaitMaxPolls && !ok; ++it) {
+            if (*abort || clock64() - t0 > kWaitBudgetCycles)
+                break;
+            __nanosleep(64);
+            ok = ld_acquire_gpu(counter) >= target;
+        }
+    }
+    if (ok)
+        fence_proxy_async_global();
+    return ok;
+}
 
 // ---------------------------------------------------------------- TMA
 // 2-D tile load global -> shared, completion counted on an mbarrier in bytes.
