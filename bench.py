@@ -93,8 +93,8 @@ def max_over_ranks(x: float, world: int) -> float:
 NCU_TRAFFIC = {
     "sources": ["w4a8_moe_gb300/csrc/moe.cu", "w4a8_moe_gb300/csrc/ptx.cuh", "w4a8_moe_gb300/csrc/sched.cuh",
                 "w4a8_moe_gb300/csrc/internal.h"],
-    "sha256": None,
-    "one_launch": None,
+    "sha256": "3c9aac6b6663792deab2dde6ceccb906e51de21b4661a740bac1e780428b30c7",
+    "one_launch": 705953536 + 4965376,
 }
 
 
