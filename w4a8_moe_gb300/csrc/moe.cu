@@ -899,7 +899,45 @@ __global__ void __launch_bounds__(256) moe_hquant_kernel(const float* __restrict
 // ---------------------------------------------------------------------------
 // Combine: out[t, n] = bf16( sum_j w[t,j] * a2 * S_d[e,n] * D ),
 // D = 512 * sum_splits P - s0h/64, in j then split order (deterministic).
+// The routing arrays come from a kernel at least two launches back and S_d
+// and a2 from no kernel of this forward (or, for the dynamic scale, two
+// launches back), so they are fetched before the dependency wait; only the
+// partial sums and s0h, which the GEMM writes, are read after it.
 // ---------------------------------------------------------------------------
+constexpr int kFinPre = 8;   // assignments per token fetched before the wait (k <= 8)
+
+template <int KS_MAX>
+__device__ __forceinline__ void fin_accumulate(float (&acc)[4], int pos, float wt, float4 sd, float a2, int A, int H,
+                                               int n, int ksplit, const float* __restrict__ ypart,
+                                               const unsigned long long* __restrict__ s0h)
+{
+    // all split partials (at most KS_MAX) are requested before the first one
+    // is added, then summed in split order
+    float4 v[KS_MAX];
+#pragma unroll
+    for (int s = 0; s < KS_MAX; ++s)
+        if (s < ksplit)
+            v[s] = __ldg(reinterpret_cast<const float4*>(ypart + (static_cast<int64_t>(s) * A + pos) * H + n));
+    const float shift = static_cast<float>(static_cast<long long>(__ldg(s0h + pos))) * (1.0f / 64.0f);
+    float4 P = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int s = 0; s < KS_MAX; ++s) {
+        if (s < ksplit) {
+            P.x += v[s].x;
+            P.y += v[s].y;
+            P.z += v[s].z;
+            P.w += v[s].w;
+        }
+    }
+    const float Pv[4] = {P.x, P.y, P.z, P.w};
+    const float Sv[4] = {sd.x, sd.y, sd.z, sd.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const float D = fmaf(512.0f, Pv[c], -shift);
+        acc[c] = fmaf(wt, a2 * Sv[c] * D, acc[c]);
+    }
+}
+
 template <int KS_MAX>
 __global__ void __launch_bounds__(256) moe_finalize_kernel(
     int T, int H, int k, int A, int ksplit, const int32_t* __restrict__ ids,
@@ -907,47 +945,43 @@ __global__ void __launch_bounds__(256) moe_finalize_kernel(
     const float* __restrict__ ypart, const unsigned long long* __restrict__ s0h,
     const float* __restrict__ s_d, const float* __restrict__ a2p, uint16_t* __restrict__ out)
 {
-    grid_dep_wait();
-    grid_dep_launch();
     const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int per_row = H / 4;
-    if (idx >= static_cast<int64_t>(T) * per_row)
-        return;
-    const int t = static_cast<int>(idx / per_row);
-    const int n = static_cast<int>(idx % per_row) * 4;
-    const float a2 = __ldg(a2p);
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < k; ++j) {
-        const int a = t * k + j;
-        const int pos = __ldg(inv + a);
-        const int e = __ldg(ids + a);
-        const float wt = __ldg(topk_w + a);
-        // all split partials (at most KS_MAX) are requested before the first
-        // one is added, then summed in split order
-        float4 v[KS_MAX];
+    const bool live = idx < static_cast<int64_t>(T) * per_row;
+    const int t = live ? static_cast<int>(idx / per_row) : 0;
+    const int n = live ? static_cast<int>(idx % per_row) * 4 : 0;
+    int pos_p[kFinPre];
+    float wt_p[kFinPre];
+    float4 sd_p[kFinPre];
+    float a2 = 0.0f;
+    if (live) {
+        a2 = __ldg(a2p);
 #pragma unroll
-        for (int s = 0; s < KS_MAX; ++s)
-            if (s < ksplit)
-                v[s] = __ldg(reinterpret_cast<const float4*>(ypart + (static_cast<int64_t>(s) * A + pos) * H + n));
-        const float shift = static_cast<float>(static_cast<long long>(__ldg(s0h + pos))) * (1.0f / 64.0f);
-        const float4 sd = __ldg(reinterpret_cast<const float4*>(s_d + static_cast<int64_t>(e) * H + n));
-        float4 P = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int s = 0; s < KS_MAX; ++s) {
-            if (s < ksplit) {
-                P.x += v[s].x;
-                P.y += v[s].y;
-                P.z += v[s].z;
-                P.w += v[s].w;
+        for (int j = 0; j < kFinPre; ++j) {
+            if (j < k) {
+                const int a = t * k + j;
+                pos_p[j] = __ldg(inv + a);
+                wt_p[j] = __ldg(topk_w + a);
+                const int e = __ldg(ids + a);
+                sd_p[j] = __ldg(reinterpret_cast<const float4*>(s_d + static_cast<int64_t>(e) * H + n));
             }
         }
-        const float Pv[4] = {P.x, P.y, P.z, P.w};
-        const float Sv[4] = {sd.x, sd.y, sd.z, sd.w};
+    }
+    grid_dep_wait();
+    grid_dep_launch();
+    if (!live)
+        return;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const float D = fmaf(512.0f, Pv[c], -shift);
-            acc[c] = fmaf(wt, a2 * Sv[c] * D, acc[c]);
-        }
+    for (int j = 0; j < kFinPre; ++j)
+        if (j < k)
+            fin_accumulate<KS_MAX>(acc, pos_p[j], wt_p[j], sd_p[j], a2, A, H, n, ksplit, ypart, s0h);
+    for (int j = kFinPre; j < k; ++j) {
+        const int a = t * k + j;
+        const int e = __ldg(ids + a);
+        fin_accumulate<KS_MAX>(acc, __ldg(inv + a), __ldg(topk_w + a),
+                               __ldg(reinterpret_cast<const float4*>(s_d + static_cast<int64_t>(e) * H + n)), a2, A,
+                               H, n, ksplit, ypart, s0h);
     }
     uint2 o;
     o.x = static_cast<uint32_t>(float_to_bf16_bits(acc[0])) |
