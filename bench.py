@@ -89,22 +89,33 @@ def max_over_ranks(x: float, world: int) -> float:
 
 # DRAM bytes (read + write) per launch of the GEMM kernel from one ncu capture
 # of the Mixtral decode layer (profiles/moe_gemm_mixtral_decode.md), valid only
-# for the GEMM sources they were taken on: a changed kernel reports null.
+# for the GEMM sources they were taken on: moe.cu without its row kernels
+# (gather, intermediate quantizer, combine: the part from "// Gather:" up to
+# "// Host side"), and the headers the GEMM includes. A changed GEMM reports null.
 NCU_TRAFFIC = {
     "sources": ["w4a8_moe_gb300/csrc/moe.cu", "w4a8_moe_gb300/csrc/ptx.cuh", "w4a8_moe_gb300/csrc/sched.cuh",
                 "w4a8_moe_gb300/csrc/internal.h"],
-    "sha256": "3c9aac6b6663792deab2dde6ceccb906e51de21b4661a740bac1e780428b30c7",
+    "sha256": "b5924027343fdbea00371e2ca73a1db77ceaf3d7d7fdffba1a45a874a19fa3e0",
     "one_launch": 705953536 + 4965376,
 }
 
 
-def ncu_traffic(kernel: str):
+def gemm_source_digest(read=None) -> str:
+    """sha256 over the GEMM's sources (see NCU_TRAFFIC)."""
     import hashlib
+    read = read or (lambda f: open(os.path.join(ROOT, f), "rb").read())
     h = hashlib.sha256()
     for f in NCU_TRAFFIC["sources"]:
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
-    return NCU_TRAFFIC.get(kernel) if h.hexdigest() == NCU_TRAFFIC["sha256"] else None
+        data = read(f)
+        if f.endswith("moe.cu"):
+            a, b = data.index(b"// Gather: "), data.index(b"// Host side")
+            data = data[:a] + data[b:]
+        h.update(data)
+    return h.hexdigest()
+
+
+def ncu_traffic(kernel: str):
+    return NCU_TRAFFIC.get(kernel) if gemm_source_digest() == NCU_TRAFFIC["sha256"] else None
 
 
 def throughput(world: int, tokens_per_rank: int, steps: int, ms_slowest: float) -> float:
