@@ -627,7 +627,9 @@ def cpu_baseline(args, shape):
     dt = time.perf_counter() - t0
     return {"value": n / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"{n} of {shape.T} tokens of the {shape.name} layer (route + exact-integer "
-                      f"MoE forward), {threads} threads"}
+                      f"MoE forward), {threads} threads",
+            "single_thread": {"value": 1.0 / one, "unit": UNIT,
+                              "sample": "token 0 of the same layer (MoE forward), 1 thread"}}
 
 
 def config_dict(shape, world):
