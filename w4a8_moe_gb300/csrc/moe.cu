@@ -67,7 +67,7 @@ struct MoeGemmParams {
     // (rows_per_expert .. ksplit) describe its gate_up tiles, these its down tiles
     int rows_per_expert2, rt_count2, kblocks2, ksplit2;
     int* done;               // [E] gate_up tiles finished per expert, x4 (one per epilogue warp)
-    int* claim;              // [2] MODE 3: tiles claimed, CTAs finished (both zero between launches)
+    int* claim;              // [2] MODE 3: tiles claimed, CTAs done claiming (both zero between launches)
     uint32_t* err;
 };
 
@@ -442,6 +442,19 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                 if (ok)   // (after a failed wait nothing more is published)
                     wi.next();
             }
+            if constexpr (MODE == 3) {
+                if (wprod) {
+                    // this CTA makes no further claim; the last CTA to get here
+                    // leaves the claim counters zero for the next launch (off
+                    // the kernel's tail: the weight stream ends before the
+                    // CTA's last tile does)
+                    __threadfence();
+                    if (atomicAdd(p.claim + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+                        atomicExch(p.claim, 0);
+                        atomicExch(p.claim + 1, 0);
+                    }
+                }
+            }
             ok = ok && wi.ok;
             if (!ok) {
                 fail();
@@ -768,18 +781,6 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
 
     tc_fence_before();
     __syncthreads();
-    if constexpr (MODE == 3) {
-        // the last CTA to finish has seen every claim of this launch: leave
-        // the claim counters zero for the next one
-        if (threadIdx.x == 0) {
-            __threadfence();
-            if (atomicAdd(p.claim + 1, 1) == static_cast<int>(gridDim.x) - 1) {
-                atomicExch(p.claim, 0);
-                atomicExch(p.claim + 1, 0);
-                __threadfence();
-            }
-        }
-    }
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
