@@ -95,8 +95,8 @@ def max_over_ranks(x: float, world: int) -> float:
 NCU_TRAFFIC = {
     "sources": ["w4a8_moe_gb300/csrc/moe.cu", "w4a8_moe_gb300/csrc/ptx.cuh", "w4a8_moe_gb300/csrc/sched.cuh",
                 "w4a8_moe_gb300/csrc/internal.h"],
-    "sha256": "b5924027343fdbea00371e2ca73a1db77ceaf3d7d7fdffba1a45a874a19fa3e0",
-    "one_launch": 705953536 + 4965376,
+    "sha256": "c958c68e525a8d1a5731dfba31c89be46f647b521f136fc81a92232f28468f36",
+    "one_launch": 705919744 + 4460544,
 }
 
 
