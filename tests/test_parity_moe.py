@@ -81,6 +81,11 @@ def test_deterministic_and_error_word_clean():
     b = case.run_gpu(ws=ws).clone()
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
     assert lib.w4a8_device_error(ws) == 0
+    # this shape runs both projections in one launch, whose tile-claim
+    # counters (header bytes 192-199) every call leaves zero for the next
+    assert lib.moe_w4a8_plan(37, 512, 512, 8, 2)["one_launch"] == 1
+    torch.cuda.synchronize()
+    assert int(ws[192:200].count_nonzero()) == 0
 
 
 def _sample_tokens(case: MoECase, n: int):
