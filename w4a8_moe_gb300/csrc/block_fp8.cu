@@ -507,8 +507,9 @@ BlkConfig blk_pick_config(int M, int N, int K, int num_sms)
     c.ksplit = 1;
     // Splitting K costs a partial round trip and a per-tile counter hand-off
     // on the fold path; measured on the block-FP8 shapes it pays only when
-    // the unsplit tiles leave most SMs idle (e.g. N = 2560 at M <= 8).
-    if (2 * base >= num_sms || M >= 64)
+    // the unsplit tiles leave most SMs idle (e.g. N = 2560 at M <= 64: 20
+    // tiles for 152 SMs). Tiles of 128 tokens are never split.
+    if (2 * base >= num_sms || c.bn >= 128)
         return c;
     const int kmax = blk_ksplit_max(M, K);
     double best_eff = 0.0;
