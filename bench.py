@@ -91,18 +91,21 @@ def max_over_ranks(x: float, world: int) -> float:
 # of the Mixtral decode layer (profiles/moe_gemm_mixtral_decode.md), valid only
 # for the GEMM sources they were taken on: moe.cu without its row kernels
 # (gather, intermediate quantizer, combine: the part from "// Gather:" up to
-# "// Host side"), and the headers the GEMM includes. A changed GEMM reports null.
+# "// Host side"), and the headers the GEMM includes, comments left out. A
+# changed GEMM reports null.
 NCU_TRAFFIC = {
     "sources": ["w4a8_moe_gb300/csrc/moe.cu", "w4a8_moe_gb300/csrc/ptx.cuh", "w4a8_moe_gb300/csrc/sched.cuh",
                 "w4a8_moe_gb300/csrc/internal.h"],
-    "sha256": "c958c68e525a8d1a5731dfba31c89be46f647b521f136fc81a92232f28468f36",
+    "sha256": "4130b854d288ead709d5c50d9e6e356976508b372508691037cea4cf94121a5a",
     "one_launch": 705919744 + 4460544,
 }
 
 
 def gemm_source_digest(read=None) -> str:
-    """sha256 over the GEMM's sources (see NCU_TRAFFIC)."""
+    """sha256 over the GEMM's sources (see NCU_TRAFFIC), comments and blank
+    lines left out (they do not change the kernel)."""
     import hashlib
+    import re
     read = read or (lambda f: open(os.path.join(ROOT, f), "rb").read())
     h = hashlib.sha256()
     for f in NCU_TRAFFIC["sources"]:
@@ -110,7 +113,10 @@ def gemm_source_digest(read=None) -> str:
         if f.endswith("moe.cu"):
             a, b = data.index(b"// Gather: "), data.index(b"// Host side")
             data = data[:a] + data[b:]
-        h.update(data)
+        text = re.sub(r"/\*.*?\*/", "", data.decode(), flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        code = "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+        h.update(code.encode())
     return h.hexdigest()
 
 

@@ -23,6 +23,12 @@
 // decode step with a handful of tokens per expert still uses M = 128 and the
 // weights stream through the SMs once.
 //
+// Launch modes (template MODE): 0 gate_up, 1 down, 2 gate_up with the
+// dynamic intermediate scale (fp32 h and max|h| out), 3 gate_up and down in
+// one launch (token tiles up to 128): the CTAs take the gate_up tiles and
+// then the down tiles, and a down tile of expert e waits on a per-expert
+// count of finished gate_up tiles, so no SM idles between the projections.
+//
 // INT4 -> E4M3 upcast. A nibble n holds q = n - 16*(n >= 8). The byte
 // o = n ^ 8 = q + 8 lies in 0..15, and the E4M3 codes 0x00..0x0F encode
 // exactly o * 2^-9 (subnormals plus the first normal binade share the spacing
