@@ -88,7 +88,7 @@ def max_over_ranks(x: float, world: int) -> float:
 
 
 # DRAM bytes (read + write) per launch of the GEMM kernel from one ncu capture
-# of the Mixtral decode layer (profiles/moe_gemm_mixtral_decode.md), valid only
+# of the Mixtral decode layer (summarized with its command under profiles/), valid only
 # for the GEMM sources they were taken on: moe.cu without its row kernels
 # (gather, intermediate quantizer, combine: the part from "// Gather:" up to
 # "// Host side"), and the headers the GEMM includes, comments left out. A
