@@ -62,6 +62,8 @@ def _load():
                 "orc_permute": (None, [P, i32, i32, i32, P, P, P, P]),
                 "orc_moe_forward": (None, [P, f32, i32, i32, i32, i32, i32, P, P, P, P, f32, i32,
                                            P, P, P, i32, P, i32]),
+                "orc_moe_hidden_codes": (None, [P, f32, i32, i32, i32, i32, i32, P, P, f32, i32, P, P,
+                                                i32, P, i32]),
                 "orc_moe_hidden_absmax": (f64, [P, f32, i32, i32, i32, i32, i32, P, P, i32, P, P,
                                                 i32, i32]),
                 "orc_block_quantize_weight": (None, [P, i32, i32, P, P]),
@@ -210,6 +212,24 @@ def moe_forward(xq, s1, w_gu, s_gu, w_d, s_d, s2, act, ids, topk_w, tokens=None,
     _load().orc_moe_forward(_p(xq), ctypes.c_float(s1), T, H, I, E, k, _p(w_gu), _p(s_gu), _p(w_d),
                             _p(s_d), ctypes.c_float(s2), int(act), _p(ids), _p(topk_w), _p(tok),
                             tok.size, _p(out), int(nthreads))
+    return out
+
+
+def moe_hidden_codes(xq, s1, w_gu, s_gu, s2, act, ids, tokens, nthreads=1) -> np.ndarray:
+    """E4M3 codes of the intermediate activation h / s2 for the listed tokens:
+    uint8 [len(tokens), k, I], assignment (token, j), i in natural order."""
+    xq = _c(xq, np.uint8)
+    T, H = xq.shape
+    w_gu = _c(w_gu, np.int32)
+    E, I2, _ = w_gu.shape
+    ids = _c(ids, np.int32)
+    k = ids.shape[1]
+    s_gu = _c(s_gu, np.float32)
+    tok = _c(tokens, np.int32)
+    out = np.empty((tok.size, k, I2 // 2), np.uint8)
+    _load().orc_moe_hidden_codes(_p(xq), ctypes.c_float(s1), T, H, I2 // 2, E, k, _p(w_gu), _p(s_gu),
+                                 ctypes.c_float(s2), int(act), _p(ids), _p(tok), tok.size, _p(out),
+                                 int(nthreads))
     return out
 
 

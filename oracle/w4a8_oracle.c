@@ -373,6 +373,7 @@ typedef struct {
     const int32_t* tokens;
     int ntok;
     double* out;        /* [ntok, H] or NULL */
+    uint8_t* hq_out;    /* [ntok, k, I] E4M3 codes of h / s2, or NULL */
     double* h_absmax;   /* per-thread slot or NULL */
     int tid, nthreads;
 } orc_moe_job;
@@ -404,7 +405,7 @@ static void* orc_moe_worker(void* arg)
             int e = J->ids[(int64_t)t * k + j];
             double wt = J->out ? J->topk_w[(int64_t)t * k + j] : 0.0;
             const int32_t* Wgu = J->w_gu + (int64_t)e * 2 * I * (H / 8);
-            const int32_t* Wd = J->w_d + (int64_t)e * H * (I / 8);
+            const int32_t* Wd = J->w_d ? J->w_d + (int64_t)e * H * (I / 8) : NULL;
             for (int i = 0; i < I; ++i) {
                 const int32_t* rg = Wgu + (int64_t)i * (H / 8);
                 const int32_t* ru = Wgu + (int64_t)(I + i) * (H / 8);
@@ -419,8 +420,12 @@ static void* orc_moe_worker(void* arg)
                 hv = orc_act(g, J->act) * u;
                 if (fabs(hv) > local_max)
                     local_max = fabs(hv);
-                if (J->out)
-                    h512[i] = orc_e4m3_times512(orc_e4m3_from_float((float)(hv / (double)J->s2)));
+                if (J->out || J->hq_out) {
+                    uint8_t code = orc_e4m3_from_float((float)(hv / (double)J->s2));
+                    h512[i] = orc_e4m3_times512(code);
+                    if (J->hq_out)
+                        J->hq_out[((int64_t)it * k + j) * I + i] = code;
+                }
             }
             if (!J->out)
                 continue;
@@ -480,6 +485,23 @@ void orc_moe_forward(const uint8_t* xq, float s1, int T, int H, int I, int E, in
     J.xq = xq; J.s1 = s1; J.T = T; J.H = H; J.I = I; J.E = E; J.k = k;
     J.w_gu = w_gu; J.s_gu = s_gu; J.w_d = w_d; J.s_d = s_d; J.s2 = s2; J.act = act;
     J.ids = ids; J.topk_w = topk_w; J.tokens = tokens; J.ntok = ntok; J.out = out;
+    orc_moe_run(&J, nthreads);
+}
+
+/* The E4M3 codes of the intermediate activation, hq[ti, j, i] =
+ * E4M3(fp32(h_i / s2)) for assignment (tokens[ti], j), i in natural order:
+ * the quantity the down projection consumes ([P1] quantization_config,
+ * static per-tensor FP8 activations), computed exactly as in
+ * orc_moe_forward. */
+void orc_moe_hidden_codes(const uint8_t* xq, float s1, int T, int H, int I, int E, int k,
+                          const int32_t* w_gu, const float* s_gu, float s2, int act, const int32_t* ids,
+                          const int32_t* tokens, int ntok, uint8_t* hq, int nthreads)
+{
+    orc_moe_job J;
+    memset(&J, 0, sizeof(J));
+    J.xq = xq; J.s1 = s1; J.T = T; J.H = H; J.I = I; J.E = E; J.k = k;
+    J.w_gu = w_gu; J.s_gu = s_gu; J.s2 = s2; J.act = act;
+    J.ids = ids; J.tokens = tokens; J.ntok = ntok; J.out = NULL; J.hq_out = hq;
     orc_moe_run(&J, nthreads);
 }
 

@@ -271,7 +271,7 @@ def _moe_case(T, H, I, E, k, act, seed, identical=False, bias=0.0):
                 sd=sd, ids=ids, tw=tw, act=act, H=H, I=I, E=E, k=k, T=T)
 
 
-def _torch_reference(c, s2, topk_w):
+def _torch_reference(c, s2, topk_w, return_codes=False):
     """Float64 torch reference on dequantized operands; library routines for the
     e4m3 conversion, the activations (silu / gelu-tanh), softmax and matmul."""
     xv = torch.from_numpy(torch_e4m3_value(c["xq"]))                      # [T,H]
@@ -279,6 +279,7 @@ def _torch_reference(c, s2, topk_w):
     qd = torch.from_numpy(oracle.unpack_int4(c["pd"]).astype(np.float64))    # [E,H,I]
     I = c["I"]
     out = torch.zeros(c["T"], c["H"], dtype=torch.float64)
+    codes = np.zeros((c["T"], c["k"], I), np.uint8)
     hmax = 0.0
     for t in range(c["T"]):
         for j in range(c["k"]):
@@ -292,9 +293,13 @@ def _torch_reference(c, s2, topk_w):
             h = a * u
             hmax = max(hmax, float(h.abs().max()))
             h32 = (h / float(s2)).to(torch.float32).clamp(-448, 448)
-            hv = h32.to(torch.float8_e4m3fn).to(torch.float64)
+            h8 = h32.to(torch.float8_e4m3fn)
+            codes[t, j] = h8.view(torch.uint8).numpy()
+            hv = h8.to(torch.float64)
             y = (qd[e] @ hv) * torch.from_numpy(c["sd"][e].astype(np.float64)) * float(s2)
             out[t] += float(topk_w[t, j]) * y
+    if return_codes:
+        return out.numpy(), hmax, codes
     return out.numpy(), hmax
 
 
@@ -311,6 +316,23 @@ def test_moe_forward_matches_float64_reference(act):
     out = oracle.moe_forward(c["xq"], c["s1"], c["pgu"], c["sgu"], c["pd"], c["sd"], s2, act,
                              c["ids"], c["tw"], nthreads=2)
     np.testing.assert_allclose(out, ref, rtol=1e-9, atol=1e-12 * np.abs(ref).max())
+
+
+@pytest.mark.parametrize("act", [0, 1])
+def test_moe_hidden_codes_match_float64_reference(act):
+    """The intermediate E4M3 codes: torch's float64 gating of dequantized
+    operands, then torch's fp32 -> float8_e4m3fn conversion of h / s2."""
+    c = _moe_case(T=5, H=256, I=128, E=3, k=2, act=act, seed=15)
+    # a scale small enough that the largest |h| saturate at +-448
+    s2 = oracle.moe_hidden_scale(c["xq"], c["s1"], c["pgu"], c["sgu"], act, c["ids"], [0]) * 0.5
+    _, _, ref = _torch_reference(c, s2, np.ones((5, 2)), return_codes=True)
+    got = oracle.moe_hidden_codes(c["xq"], c["s1"], c["pgu"], c["sgu"], s2, act, c["ids"],
+                                  [0, 1, 2, 3, 4], nthreads=2)
+    assert got.shape == (5, 2, 128)
+    assert np.array_equal(got, ref)
+    assert np.any((got & 0x7F) == 0x7E)                         # saturated codes present
+    sub = oracle.moe_hidden_codes(c["xq"], c["s1"], c["pgu"], c["sgu"], s2, act, c["ids"], [3, 1])
+    assert np.array_equal(sub, got[[3, 1]])
 
 
 def test_moe_single_expert_is_dense_mlp():
