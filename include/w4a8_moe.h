@@ -152,7 +152,7 @@ size_t moe_route_gate_workspace_size(int T, int H, int E, int k);
  *   gate_i = a1 * S_gu[e, i]     * sum_h x[t,h] q_gu[e, i, h]         (i < I)
  *   up_i   = a1 * S_gu[e, I + i] * sum_h x[t,h] q_gu[e, I + i, h]
  *   h_i    = act(gate_i) * up_i,  act = SiLU (act = 0) or GELU-tanh (act = 1)
- *   hq_i   = E4M3(h_i / a2)                                    (static scale a2)
+ *   hq_i   = E4M3(h_i / a2)     (static scale a2; IEEE fp32 division, one RNE rounding)
  *   y_n    = a2 * S_d[e, n] * sum_i hq_i q_d[e, n, i]
  *   out[t, n] = bf16( sum_j topk_w[t, j] * y_n(t, j) )
  * with x = dec(x_e4m3) and fp32 tensor-core accumulation.
@@ -203,6 +203,24 @@ size_t moe_w4a8_workspace_size(int T, int H, int I, int E, int k);
 int moe_w4a8_plan(int T, int H, int I, int E, int k, int dynamic, int num_sms, int32_t* plan);
 
 /*
+ * moe_w4a8_workspace_layout -- inspection hook (the pages have no
+ * counterpart): where, inside the workspace of moe_w4a8_forward or
+ * moe_w4a8_forward_dynamic for this shape, a call leaves its intermediate
+ * tensors, so that tests can compare them with a reference. Host only.
+ *
+ *   offsets [2] int64 (host), out: byte offsets from the workspace start of
+ *     [0] hq [T*k, I] u8: the E4M3 codes of h / a2. Row p holds assignment
+ *         a = sorted_ids[p] (token a / k, slot a % k); inside every group of
+ *         8 columns the codes of i = 8g + {0, 2, 4, 6, 1, 3, 5, 7}, the K
+ *         order the down projection consumes.
+ *     [1] xp [T*k, H] u8: the gathered E4M3 activations, same row and
+ *         column orders.
+ *   Returns W4A8_ERR_SHAPE for shapes moe_w4a8_forward rejects,
+ *   W4A8_ERR_NULL for a null offsets.
+ */
+int moe_w4a8_workspace_layout(int T, int H, int I, int E, int k, int64_t* offsets);
+
+/*
  * moe_w4a8_forward_dynamic -- moe_w4a8_forward with the intermediate
  * activation's scale calibrated on the device for every call instead of read:
  *   a2 = max |h_i| / 448 over every assignment and i of the call (1 when all
@@ -234,22 +252,28 @@ size_t moe_w4a8_dynamic_workspace_size(int T, int H, int I, int E, int k);
  * moment). This entry point takes the same inputs and outputs as
  * moe_w4a8_forward, minus ws/ws_bytes, and uses instead a scratch array of
  * W4A8_STATIC_SCRATCH_BYTES that lives in the library's own device image: every
- * GPU that loads the library reserves it until the process exits. It calls no
- * allocating function.
+ * CUDA context that loads the library reserves it until the process exits. It
+ * calls no allocating function.
  *
- *   - Problems whose moe_w4a8_workspace_size(T, H, I, E, k) exceeds
- *     W4A8_STATIC_SCRATCH_BYTES return W4A8_ERR_WORKSPACE (use
- *     moe_w4a8_forward with a caller workspace for those); that covers
- *     decode-sized layers (e.g. 32 tokens of a Grok-1-shaped layer).
- *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture on the device.
- *   - All calls on a device share the one array and it keeps the last call's
+ *   - Arguments are checked as moe_w4a8_forward checks them (W4A8_ERR_NULL,
+ *     W4A8_ERR_SHAPE, W4A8_ERR_ALIGN, in that order); then problems whose
+ *     moe_w4a8_workspace_size(T, H, I, E, k) exceeds W4A8_STATIC_SCRATCH_BYTES
+ *     return W4A8_ERR_WORKSPACE (use moe_w4a8_forward with a caller workspace
+ *     for those); the limit covers decode-sized layers (e.g. 32 tokens of a
+ *     Grok-1-shaped layer, or 128 tokens of a Mixtral-shaped one).
+ *   - The first call in a CUDA context (the device's primary context, or a
+ *     context the application made current) looks up the array's device
+ *     address in that context (cudaGetSymbolAddress) and caches it under the
+ *     context handle; make that first call before any stream capture. A
+ *     context that is destroyed must not be followed by a new context at the
+ *     same handle in the same process.
+ *   - All calls in a context share the one array and it keeps the last call's
  *     contents; the state each call needs cleared is cleared by the call's
  *     first kernel. Calls whose kernels overlap on the GPU (concurrent streams,
  *     or host threads using the same device) race on the array: serialize
  *     them, e.g. on one stream.
- *   - A bounded device wait that runs out is not reported by this variant.
+ *   - A bounded device wait that runs out sets the array's error word (as it
+ *     would a workspace's); moe_w4a8_forward_static_error reads and clears it.
  */
 #define W4A8_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
 int moe_w4a8_forward_static(const uint8_t* x_e4m3, const float* a1_scale, int T, int H, int I,
@@ -258,6 +282,16 @@ int moe_w4a8_forward_static(const uint8_t* x_e4m3, const float* a1_scale, int T,
                             const int32_t* topk_ids, const float* topk_w, const int32_t* counts,
                             const int32_t* offsets, const int32_t* sorted_ids,
                             const int32_t* inv_perm, uint16_t* out_bf16, void* stream);
+
+/*
+ * moe_w4a8_forward_static_error -- w4a8_device_error for the built-in scratch
+ * array of moe_w4a8_forward_static in the current context: *code_out receives
+ * W4A8_OK, or W4A8_ERR_TIMEOUT when one of its kernels gave up on a bounded
+ * wait since the last read; the word is cleared. Synchronizes `stream`.
+ * Allocates nothing. Returns W4A8_OK, W4A8_ERR_NULL, W4A8_ERR_DEVICE or
+ * W4A8_ERR_LAUNCH.
+ */
+int moe_w4a8_forward_static_error(int* code_out, void* stream);
 
 /*
  * fp8_linear -- per-tensor FP8 dense projection ("[AMD][Quantization] Add

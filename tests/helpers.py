@@ -52,10 +52,62 @@ def compare(got: np.ndarray, ref: np.ndarray):
     return float(rel), float(mabs)
 
 
-def assert_close(got, ref, what=""):
+# Every comparison made by assert_close, for the margin table that
+# tests/conftest.py prints at the end of the session.
+MARGINS = []
+
+
+def assert_close(got, ref, what="", bf16_out=True):
+    """rel-L2 and max-abs of `got` against the oracle's float64 `ref`, within
+    the parity bar. For a bf16 output also reports the same two measures
+    against the oracle result rounded once to bf16: that part of the error is
+    the kernel's own (the output format's rounding is no longer in it)."""
     rel, mabs = compare(got, ref)
+    row = {"what": what, "rel_l2": rel, "max_abs": mabs, "n": int(np.asarray(ref).size)}
+    if bf16_out:
+        ref_b = oracle.bf16_to_float(oracle.bf16_from_double(np.asarray(ref, np.float64)))
+        rb, mb = compare(got, ref_b)
+        row.update(rel_l2_vs_bf16_ref=rb, max_abs_vs_bf16_ref=mb,
+                   bf16_flips=float(np.mean(np.asarray(got, np.float64) != ref_b.astype(np.float64))))
+    MARGINS.append(row)
+    print(f"[margin] {what}: rel_l2={rel:.3e} (bar {REL_L2_TOL:.0e}) max_abs/max|ref|={mabs:.3e} "
+          f"(bar {MAX_ABS_TOL:.0e})"
+          + (f"; vs bf16(ref): rel_l2={row['rel_l2_vs_bf16_ref']:.3e} "
+             f"flips={row['bf16_flips']:.3%}" if bf16_out else ""))
     assert rel <= REL_L2_TOL and mabs <= MAX_ABS_TOL, f"{what}: rel_l2={rel:.3e} max_abs/max|ref|={mabs:.3e}"
     return rel, mabs
+
+
+def kperm_index(n: int) -> np.ndarray:
+    """Column of element i in the library's stored K order: inside every group
+    of 8, elements 0,2,4,6 then 1,3,5,7 (include/w4a8_moe.h,
+    moe_w4a8_workspace_layout)."""
+    i = np.arange(n)
+    return (i & ~7) | ((i & 7) >> 1) | ((i & 1) << 2)
+
+
+def e4m3_step_index(codes: np.ndarray) -> np.ndarray:
+    """Signed position of an E4M3 code on the ordered grid of finite values
+    (+0 and -0 both 0): two codes are neighbours iff positions differ by 1."""
+    c = np.asarray(codes, np.int64)
+    mag = c & 0x7F
+    return np.where(c & 0x80, -mag, mag)
+
+
+def compare_codes(got: np.ndarray, ref: np.ndarray, what=""):
+    """E4M3 codes of the intermediate activation: the share that differ and
+    whether every difference is one step of the E4M3 grid (a value of h / a2
+    near a rounding midpoint, decided on either side of it by the kernel's fp32
+    arithmetic and the oracle's exact sums)."""
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    diff = got != ref
+    rate = float(diff.mean())
+    far = int((np.abs(e4m3_step_index(got) - e4m3_step_index(ref)) > 1).sum())
+    MARGINS.append({"what": what + " (hq codes)", "code_mismatch_rate": rate, "non_adjacent": far,
+                    "n": int(ref.size)})
+    print(f"[margin] {what}: hq code mismatches {int(diff.sum())} of {ref.size} ({rate:.2e}), "
+          f"non-adjacent {far}")
+    return rate, far
 
 
 def oracle_threads() -> int:
@@ -78,7 +130,7 @@ class MoECase:
     """One MoE layer run through both sides on the same seeded inputs."""
 
     def __init__(self, T, H, I, E, k, act, bias_std=0.0, seed=0, logits_override=None,
-                 calib_tokens=8, weights=None):
+                 calib_tokens=256, weights=None):
         import w4a8_moe_gb300 as lib
         self.T, self.H, self.I, self.E, self.k, self.act = T, H, I, E, k, act
         inp = synth.moe_inputs(T, H, I, E, bias_std=bias_std, seed=seed, device="cuda",
@@ -113,6 +165,22 @@ class MoECase:
                                    self.a2, self.act, self.route, ws=ws)
         torch.cuda.synchronize()
         return out
+
+    def gpu_hidden_codes(self, ws) -> np.ndarray:
+        """The kernel's E4M3 intermediate codes left in `ws` by the last forward
+        call, as uint8 [T, k, I] in natural i order."""
+        import w4a8_moe_gb300 as lib
+        off = lib.moe_w4a8_workspace_layout(self.T, self.H, self.I, self.E, self.k)["hq"]
+        A = self.T * self.k
+        rows = ws[off:off + A * self.I].view(A, self.I).cpu().numpy()
+        nat = rows[:, kperm_index(self.I)]
+        out = np.empty((A, self.I), np.uint8)
+        out[self.o_sorted] = nat
+        return out.reshape(self.T, self.k, self.I)
+
+    def oracle_hidden_codes(self, tokens):
+        return oracle.moe_hidden_codes(self.o_xq, self.o_s1, self.o_pgu, self.o_sgu, self.s2, self.act,
+                                       self.o_ids, tokens, nthreads=oracle_threads())
 
     def oracle_out(self, tokens=None):
         return oracle.moe_forward(self.o_xq, self.o_s1, self.o_pgu, self.o_sgu, self.o_pd, self.o_sd,

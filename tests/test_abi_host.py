@@ -201,3 +201,45 @@ def test_plan_fits_the_workspace(lib):
                     ws = lib.moe_w4a8_workspace_size(T, H, I, E, k)
                     assert ws >= p[7] * T * k * H * 4, (T, H, I, E, k, dyn, sms, p)
                     assert p[5] in (0, 1) and (p[5] == 0 or (dyn == 0 and p[0] <= 128))
+
+
+def test_static_scratch_forward_checks_like_the_regular_one(lib):
+    """moe_w4a8_forward_static: the regular entry point's null / shape /
+    alignment statuses in the same order, then W4A8_ERR_WORKSPACE for a
+    problem larger than the built-in array, all without a device."""
+    P, i32 = ctypes.c_void_p, ctypes.c_int
+    f = lib.moe_w4a8_forward_static
+    f.argtypes = [P, P, i32, i32, i32, i32, i32, P, P, P, P, P, i32, P, P, P, P, P, P, P, P]
+    f.restype = i32
+    g = _vp(0x10000)
+    args = lambda T, H, I, E, k, act=0, x=g: [x, g, T, H, I, E, k, g, g, g, g, g, act, g, g, g, g, g, g, g, None]
+    assert f(*args(32, 4096, 14336, 8, 2, x=None)) == 1          # NULL before anything else
+    assert f(*args(0, 4096, 14336, 8, 2)) == 2                   # T < 1: shape, as the regular call
+    assert f(*args(32, -256, 14336, 8, 2)) == 2
+    assert f(*args(32, 4096, 14336, 8, 2, act=5)) == 2
+    assert f(*args(32, 4096, 14336, 8, 2, x=_vp(0x10001))) == 3  # alignment
+    assert f(*args(32768, 6144, 32768, 8, 2)) == 4               # needs gigabytes of scratch
+    if not torch.cuda.is_available():
+        assert f(*args(32, 4096, 14336, 8, 2)) == 5              # fits, but no sm_103 device
+    e = lib.moe_w4a8_forward_static_error
+    e.argtypes = [P, P]
+    e.restype = i32
+    assert e(None, None) == 1
+
+
+def test_workspace_layout_hook(lib):
+    """The intermediate codes sit inside the workspace the size query promises."""
+    i64 = ctypes.c_int64
+    f = lib.moe_w4a8_workspace_layout
+    f.argtypes = [ctypes.c_int] * 5 + [ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    lib.moe_w4a8_workspace_size.restype = ctypes.c_size_t
+    for (T, H, I, E, k) in ((16, 256, 512, 8, 2), (32, 4096, 14336, 8, 2), (300, 256, 256, 8, 2)):
+        off = (i64 * 2)()
+        assert f(T, H, I, E, k, ctypes.cast(off, ctypes.c_void_p)) == 0
+        hq, xp = off[0], off[1]
+        ws = lib.moe_w4a8_workspace_size(T, H, I, E, k)
+        assert 256 <= xp and xp + T * k * H <= hq and hq + T * k * I <= ws
+        assert hq % 256 == 0 and xp % 256 == 0
+    assert f(0, 256, 512, 8, 2, ctypes.cast((i64 * 2)(), ctypes.c_void_p)) == 2
+    assert f(16, 256, 512, 8, 2, None) == 1

@@ -5,7 +5,7 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import MoECase, QuantizedWeights, assert_close, bf16_to_f64, ensure_built
+from helpers import MoECase, QuantizedWeights, assert_close, bf16_to_f64, compare_codes, ensure_built
 from w4a8_moe_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -27,7 +27,11 @@ def run_case(case: MoECase, tokens=None, what=""):
 def test_tiny_layer_all_tokens():
     s = synth.MOE_SHAPES["tiny"]
     case = MoECase(s.T, s.H, s.I, s.E, s.k, s.act)
-    run_case(case, what="tiny")
+    case.check_integer_parts()
+    ws = _workspace(case)
+    out = case.run_gpu(ws=ws)
+    check_hidden_codes(case, ws, list(range(s.T)), "tiny")
+    assert_close(bf16_to_f64(out), case.oracle_out(), "tiny")
 
 
 @pytest.mark.parametrize("T,H,I,E,k,act", [
@@ -88,32 +92,57 @@ def test_deterministic_and_error_word_clean():
     assert int(ws[192:200].count_nonzero()) == 0
 
 
-def _sample_tokens(case: MoECase, n: int):
-    """A few tokens that between them touch the most and the least loaded expert."""
-    ids = case.o_ids
-    counts = case.o_counts
-    live = [e for e in range(case.E) if counts[e] > 0]
+def covering_sample(case: MoECase, n: int, seed: int = 0):
+    """A seeded sample of n tokens that covers every expert with tokens: first
+    one token of each expert, least loaded expert first, then random tokens,
+    and the last token of the batch."""
+    ids, counts = case.o_ids, case.o_counts
     pick = []
-    for e in (min(live, key=lambda e: counts[e]), max(live, key=lambda e: counts[e])):
-        t = int(np.nonzero((ids == e).any(1))[0][-1])
-        if t not in pick:
-            pick.append(t)
-    rng = np.random.default_rng(0)
+    for e in sorted((e for e in range(case.E) if counts[e] > 0), key=lambda e: (counts[e], e)):
+        routed = np.nonzero((ids == e).any(1))[0]
+        if not any(t in pick for t in routed.tolist()):
+            pick.append(int(routed[-1]))
+    if case.T - 1 not in pick:
+        pick.append(case.T - 1)
+    rng = np.random.default_rng(seed)
     for t in rng.permutation(case.T):
         if len(pick) >= n:
             break
         if int(t) not in pick:
             pick.append(int(t))
-    return sorted(pick)
+    toks = sorted(pick)
+    covered = set(ids[toks].ravel().tolist())
+    assert covered == {e for e in range(case.E) if counts[e] > 0}
+    return toks
+
+
+def check_hidden_codes(case: MoECase, ws, tokens, what, max_rate=1e-3):
+    """The kernel's intermediate E4M3 codes against the oracle's, on the
+    sampled tokens: a small share may sit one E4M3 step apart (h / a2 within
+    fp32 rounding of a midpoint); none further."""
+    got = case.gpu_hidden_codes(ws)[tokens]
+    ref = case.oracle_hidden_codes(tokens)
+    rate, far = compare_codes(got, ref, what)
+    assert far == 0, f"{what}: {far} intermediate codes more than one E4M3 step from the oracle's"
+    assert rate <= max_rate, f"{what}: intermediate code mismatch rate {rate:.2e}"
+
+
+def _workspace(case: MoECase):
+    import w4a8_moe_gb300 as lib
+    return torch.zeros(lib.moe_w4a8_workspace_size(case.T, case.H, case.I, case.E, case.k),
+                       dtype=torch.uint8, device="cuda")
 
 
 def test_mixtral_decode_full_size():
+    """All 32 tokens of the Mixtral-shaped decode layer, and every intermediate code."""
     s = synth.MOE_SHAPES["mixtral_decode"]
     case = MoECase(s.T, s.H, s.I, s.E, s.k, s.act, bias_std=s.bias_std)
     case.check_integer_parts()
-    toks = _sample_tokens(case, 6)
-    out = case.run_gpu()
-    assert_close(bf16_to_f64(out[toks]), case.oracle_out(toks), "mixtral decode")
+    ws = _workspace(case)
+    out = case.run_gpu(ws=ws)
+    toks = list(range(s.T))
+    check_hidden_codes(case, ws, toks, "mixtral decode")
+    assert_close(bf16_to_f64(out), case.oracle_out(toks), "mixtral decode T32")
 
 
 @pytest.fixture(scope="module")
@@ -128,20 +157,30 @@ def grok_weights():
 
 @pytest.mark.parametrize("name", ["grok_decode", "grok_decode_t8", "grok_decode_t1"])
 def test_grok_decode_full_size(name, grok_weights):
+    """Every token of the Grok-1-shaped decode layers (32, 8 and 1 tokens)."""
     s = synth.MOE_SHAPES[name]
     case = MoECase(s.T, s.H, s.I, s.E, s.k, s.act, bias_std=s.bias_std, weights=grok_weights)
     case.check_integer_parts(sample_rows=[(0, 0), (3, 40000), (7, 65535)])
-    toks = _sample_tokens(case, 3)
-    out = case.run_gpu()
-    assert_close(bf16_to_f64(out[toks]), case.oracle_out(toks), name)
+    ws = _workspace(case)
+    out = case.run_gpu(ws=ws)
+    toks = list(range(s.T))
+    check_hidden_codes(case, ws, toks, name)
+    assert_close(bf16_to_f64(out), case.oracle_out(toks), name)
 
 
 def test_grok_prefill_full_size_sampled(grok_weights):
+    """The 32768-token Grok-1 prefill layer: route and permutation on every
+    token (bit-exact), the output and the intermediate codes on a seeded
+    512-token sample that covers every expert, the least loaded included
+    (each token's output depends only on that token, given the static scales)."""
     s = synth.MOE_SHAPES["grok_prefill"]
     case = MoECase(s.T, s.H, s.I, s.E, s.k, s.act, bias_std=s.bias_std, weights=grok_weights)
     case.check_integer_parts(sample_rows=[(1, 5)])
     assert case.o_counts.max() > 2 * case.o_counts.min()       # skewed load
-    toks = _sample_tokens(case, 4) + [s.T - 1]
-    out = case.run_gpu()
+    toks = covering_sample(case, 512)
+    assert len(toks) == 512
+    ws = _workspace(case)
+    out = case.run_gpu(ws=ws)
     assert torch.isfinite(out.float()).all()
-    assert_close(bf16_to_f64(out[toks]), case.oracle_out(toks), "grok prefill")
+    check_hidden_codes(case, ws, toks, "grok prefill (512-token sample)")
+    assert_close(bf16_to_f64(out[toks]), case.oracle_out(toks), "grok prefill (512-token sample)")

@@ -20,7 +20,8 @@ __all__ = [
     "fp8_block_linear", "w4a8_device_error", "w4a8_selftest_wait_timeout", "w4a8_set_profile_events", "moe_w4a8_workspace_size",
     "moe_route_workspace_size", "fp8_block_linear_workspace_size", "moe_route_gate",
     "moe_route_gate_workspace_size", "fp8_linear", "fp8_linear_workspace_size",
-    "moe_w4a8_forward_dynamic", "moe_w4a8_dynamic_workspace_size",
+    "moe_w4a8_forward_dynamic", "moe_w4a8_dynamic_workspace_size", "moe_w4a8_workspace_layout",
+    "moe_w4a8_plan",
     "w4a8_quantize_act_workspace_size", "RouteResult", "library_path", "W4A8Error",
 ]
 
@@ -62,6 +63,7 @@ def _load():
                                    P, P, P, sz, P]),
         "moe_w4a8_workspace_size": (sz, [i32, i32, i32, i32, i32]),
         "moe_w4a8_plan": (i32, [i32, i32, i32, i32, i32, i32, i32, P]),
+        "moe_w4a8_workspace_layout": (i32, [i32, i32, i32, i32, i32, P]),
         "moe_w4a8_forward_dynamic": (i32, [P, P, i32, i32, i32, i32, i32, P, P, P, P, P, i32, P, P, P, P, P,
                                            P, P, P, sz, P]),
         "moe_w4a8_dynamic_workspace_size": (sz, [i32, i32, i32, i32, i32]),
@@ -125,6 +127,14 @@ def moe_w4a8_plan(T, H, I, E, k, dynamic=False, num_sms=None) -> dict:
     plan = (ctypes.c_int32 * 8)()
     _check(_load().moe_w4a8_plan(T, H, I, E, k, 1 if dynamic else 0, num_sms, plan))
     return dict(zip(_PLAN_KEYS, list(plan)))
+
+
+def moe_w4a8_workspace_layout(T, H, I, E, k) -> dict:
+    """Byte offsets of the intermediate tensors a forward call leaves in its
+    workspace (see moe_w4a8_workspace_layout in include/w4a8_moe.h)."""
+    off = (ctypes.c_int64 * 2)()
+    _check(_load().moe_w4a8_workspace_layout(T, H, I, E, k, off))
+    return {"hq": int(off[0]), "xp": int(off[1])}
 
 
 def moe_w4a8_dynamic_workspace_size(T, H, I, E, k) -> int:

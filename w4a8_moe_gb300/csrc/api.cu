@@ -359,6 +359,20 @@ size_t moe_w4a8_workspace_size(int T, int H, int I, int E, int k)
     return moe_ws(T, H, I, k, &w, nullptr);
 }
 
+int moe_w4a8_workspace_layout(int T, int H, int I, int E, int k, int64_t* offsets)
+{
+    if (!offsets)
+        return W4A8_ERR_NULL;
+    if (!moe_shape_ok(T, H, I, E, k))
+        return W4A8_ERR_SHAPE;
+    MoeWs w;
+    moe_ws(T, H, I, k, &w, reinterpret_cast<void*>(static_cast<uintptr_t>(kAlign)));
+    // moe_ws carves from a non-null base; offsets are relative to it
+    offsets[0] = static_cast<int64_t>(reinterpret_cast<uintptr_t>(w.hq) - kAlign);
+    offsets[1] = static_cast<int64_t>(reinterpret_cast<uintptr_t>(w.xp) - kAlign);
+    return W4A8_OK;
+}
+
 int moe_w4a8_plan(int T, int H, int I, int E, int k, int dynamic, int num_sms, int32_t* plan)
 {
     if (!plan)
@@ -381,6 +395,20 @@ int moe_w4a8_plan(int T, int H, int I, int E, int k, int dynamic, int num_sms, i
 
 }  // extern "C"
 
+// Checks of moe_w4a8_forward that need no workspace: pointers, shape, alignment.
+int w4a8::moe_forward_check(const void* const* ptrs, int nptrs, int T, int H, int I, int E, int k, int act)
+{
+    for (int i = 0; i < nptrs; ++i)
+        if (!ptrs[i])
+            return W4A8_ERR_NULL;
+    if (!moe_shape_ok(T, H, I, E, k) || (act != 0 && act != 1))
+        return W4A8_ERR_SHAPE;
+    for (int i = 0; i < nptrs; ++i)
+        if (!aligned16(ptrs[i]))
+            return W4A8_ERR_ALIGN;
+    return W4A8_OK;
+}
+
 // The MoE forward with a static (a2_scale read) or dynamic (computed from the
 // call's h and written to a2_out) intermediate scale.
 static int moe_forward_common(const uint8_t* x_e4m3, const float* a1_scale, int T, int H, int I, int E, int k,
@@ -392,14 +420,8 @@ static int moe_forward_common(const uint8_t* x_e4m3, const float* a1_scale, int 
 {
     const void* ptrs[] = {x_e4m3, a1_scale, w_gu, s_gu, w_d, s_d, a2_scale, topk_ids, topk_w,
                           counts, offsets, sorted_ids, inv_perm, out_bf16};
-    for (const void* p : ptrs)
-        if (!p)
-            return W4A8_ERR_NULL;
-    if (!moe_shape_ok(T, H, I, E, k) || (act != 0 && act != 1))
-        return W4A8_ERR_SHAPE;
-    for (const void* p : ptrs)
-        if (!aligned16(p))
-            return W4A8_ERR_ALIGN;
+    if (int st = moe_forward_check(ptrs, 14, T, H, I, E, k, act))
+        return st;
     if (!ws || ws_bytes < (dynamic ? moe_w4a8_dynamic_workspace_size(T, H, I, E, k)
                                   : moe_w4a8_workspace_size(T, H, I, E, k)))
         return W4A8_ERR_WORKSPACE;

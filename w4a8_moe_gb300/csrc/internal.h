@@ -88,6 +88,9 @@ struct MoeLaunch {
     void* events[4];  // optional cudaEvent_t recorded around the GEMMs
 };
 int launch_moe_forward(const MoeLaunch& L, const MoeConfig& cfg, int num_sms, cudaStream_t s);
+// The checks moe_w4a8_forward makes before it looks at the workspace, in the
+// same order (null pointers, shape, alignment); returns a public status code.
+int moe_forward_check(const void* const* ptrs, int nptrs, int T, int H, int I, int E, int k, int act);
 
 // ---- block_fp8.cu
 struct BlkConfig {

@@ -631,7 +631,7 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
         grid_dep_wait();
         grid_dep_launch();
         const float a1 = __ldg(p.a1);
-        const float inv_a2 = 1.0f / __ldg(p.a2);
+        const float a2 = __ldg(p.a2);
         uint32_t gsum = 0;   // global stage index of the tile's first stage
         int it = 0;
         bool ok = true;
@@ -707,7 +707,8 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                                 p.hf[static_cast<int64_t>(pos) * p.I + i] = h;
                                 hmax_l = fmaxf(hmax_l, fabsf(h));
                             } else {
-                                const uint32_t code = cvt_e4m3(h * inv_a2);
+                                // hq = E4M3(h / a2): IEEE division, then one RNE rounding
+                                const uint32_t code = cvt_e4m3(__fdiv_rn(h, a2));
                                 p.hq[static_cast<int64_t>(pos) * p.I + kperm(i)] = static_cast<uint8_t>(code);
                                 s512[cc] = e4m3_times512(code);
                             }
@@ -852,7 +853,7 @@ __global__ void __launch_bounds__(128) moe_gather_kernel(const uint8_t* __restri
 
 // ---------------------------------------------------------------------------
 // Dynamic intermediate scale: a2 = max|h| / 448 over every assignment of the
-// call (1 if all h are zero), then hq = E4M3(h / a2) in the permuted K order
+// call (1 if all h are zero), then hq = E4M3(h / a2) (IEEE division) in the permuted K order
 // of unpack8 and the exact row sums s0h[pos] = sum_i 512*dec(hq). One block per
 // assignment row; 8 consecutive h per thread.
 // ---------------------------------------------------------------------------
@@ -867,7 +868,6 @@ __global__ void __launch_bounds__(256) moe_hquant_kernel(const float* __restrict
     __shared__ long long red[8];
     const float mx = __uint_as_float(__ldcg(hmax));
     const float s2 = (mx > 0.0f && mx <= 3.4028234663852886e38f) ? __fdiv_rn(mx, 448.0f) : 1.0f;
-    const float inv = 1.0f / s2;
     if (blockIdx.x == 0 && threadIdx.x == 0)
         *a2_out = s2;
     const int pos = blockIdx.x;
@@ -880,7 +880,7 @@ __global__ void __launch_bounds__(256) moe_hquant_kernel(const float* __restrict
         uint32_t c[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            c[j] = cvt_e4m3(h[j] * inv);
+            c[j] = cvt_e4m3(__fdiv_rn(h[j], s2));
             sum += e4m3_times512(c[j]);
         }
         // byte order inside the group: elements 0,2,4,6 then 1,3,5,7

@@ -120,6 +120,6 @@ def fp8_linear_inputs(M: int, N: int, K: int, seed: int = 0, device="cpu", weigh
     return {"x": x.contiguous(), "w": w.contiguous()}
 
 
-def calibration_tokens(T: int, n: int = 8):
+def calibration_tokens(T: int, n: int = 256):
     """Tokens the static intermediate scale is calibrated on: the first min(T, n)."""
     return list(range(min(T, n)))
