@@ -140,6 +140,9 @@ def test_workspace_sizes_are_monotone(lib):
     assert 256 < a < b
     # decode: hq + gathered x + split-K partials; prefill-sized grows with T
     assert lib.moe_w4a8_workspace_size(32768, 6144, 32768, 8, 2) > 4 * 10**9
+    # prefill-sized calls hold the weights unpacked once: E * 3 * I * H bytes more
+    assert lib.moe_w4a8_workspace_size(129, 512, 256, 8, 2) - lib.moe_w4a8_workspace_size(128, 512, 256, 8, 2) \
+        >= 8 * 3 * 256 * 512
     assert lib.fp8_block_linear_workspace_size(1, 16384, 2560) > 2560
 
 
@@ -163,7 +166,8 @@ def _plan(lib, T, H, I, E, k, dynamic=0, sms=152):
 def test_plan_of_the_decode_and_prefill_layers(lib):
     """The host planner (no GPU needed): decode-sized layers with the static
     scale run both projections in one launch, the dynamic scale and the
-    256-token tiles of a prefill run them separately."""
+    256-token tiles of a prefill run them separately, after unpacking the
+    weights once."""
     st, p = _plan(lib, 32, 4096, 14336, 8, 2)                  # Mixtral decode
     assert st == 0 and p[0] == 32 and p[5] == 1 and p[6] == 3
     assert (14336 // p[1]) % p[2] == 0 and p[7] == p[2] and p[3] == 0
@@ -172,7 +176,7 @@ def test_plan_of_the_decode_and_prefill_layers(lib):
     st, p = _plan(lib, 1, 6144, 32768, 8, 2)                   # Grok single token
     assert st == 0 and p[5] == 1 and p[2] > 1                   # the down K is split to fill the SMs
     st, p = _plan(lib, 32768, 6144, 32768, 8, 2)               # Grok prefill
-    assert st == 0 and p[0] == 256 and p[5] == 0 and p[6] == 4 and p[7] == 1
+    assert st == 0 and p[0] == 256 and p[5] == 0 and p[6] == 5 and p[7] == 1   # + the weights' unpack
 
 
 def test_plan_rejects_what_the_forward_rejects(lib):

@@ -144,8 +144,9 @@ struct MoeWs {
     float* hf;             // dynamic intermediate scale only
     unsigned int* hmax;    // header word at byte 64 (dynamic only)
     int* done;             // [256] per-expert progress counters (one-launch forward)
+    uint8_t* wq8;          // prefill: the weights unpacked once per call
 };
-static size_t moe_ws(int T, int H, int I, int k, MoeWs* w, void* ws, bool dynamic = false)
+static size_t moe_ws(int T, int H, int I, int E, int k, MoeWs* w, void* ws, bool dynamic = false)
 {
     Carver c(ws);
     const size_t A = static_cast<size_t>(T) * k;
@@ -156,6 +157,7 @@ static size_t moe_ws(int T, int H, int I, int k, MoeWs* w, void* ws, bool dynami
     w->ypart = c.take<float>(static_cast<size_t>(moe_ksplit_max(T, k)) * A * H * 4);
     w->hf = c.take<float>(dynamic ? A * I * 4 : 0);
     w->done = c.take<int>(256 * 4);
+    w->wq8 = c.take<uint8_t>(moe_unpack_once(T) ? static_cast<size_t>(E) * 3 * I * H : 0);
     w->hmax = ws ? reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + 64) : nullptr;
     return c.off;
 }
@@ -354,9 +356,8 @@ int moe_route(const float* logits, int T, int E, int k, int renormalize, int32_t
 
 size_t moe_w4a8_workspace_size(int T, int H, int I, int E, int k)
 {
-    (void)E;
     MoeWs w;
-    return moe_ws(T, H, I, k, &w, nullptr);
+    return moe_ws(T, H, I, E, k, &w, nullptr);
 }
 
 int moe_w4a8_workspace_layout(int T, int H, int I, int E, int k, int64_t* offsets)
@@ -366,7 +367,7 @@ int moe_w4a8_workspace_layout(int T, int H, int I, int E, int k, int64_t* offset
     if (!moe_shape_ok(T, H, I, E, k))
         return W4A8_ERR_SHAPE;
     MoeWs w;
-    moe_ws(T, H, I, k, &w, reinterpret_cast<void*>(static_cast<uintptr_t>(kAlign)));
+    moe_ws(T, H, I, E, k, &w, reinterpret_cast<void*>(static_cast<uintptr_t>(kAlign)));
     // moe_ws carves from a non-null base; offsets are relative to it
     offsets[0] = static_cast<int64_t>(reinterpret_cast<uintptr_t>(w.hq) - kAlign);
     offsets[1] = static_cast<int64_t>(reinterpret_cast<uintptr_t>(w.xp) - kAlign);
@@ -387,8 +388,9 @@ int moe_w4a8_plan(int T, int H, int I, int E, int k, int dynamic, int num_sms, i
     plan[3] = one ? 0 : c.streamk;
     plan[4] = one ? 0 : c.nslots;
     plan[5] = one ? 1 : 0;
-    // gather, the GEMM launch(es), the dynamic scale's quantizer, the combine
-    plan[6] = 1 + (one ? 1 : 2) + (dynamic ? 1 : 0) + 1;
+    // the prefill unpack, the gather, the GEMM launch(es), the dynamic scale's
+    // quantizer, the combine
+    plan[6] = (c.a8 ? 1 : 0) + 1 + (one ? 1 : 2) + (dynamic ? 1 : 0) + 1;
     plan[7] = (one || !c.streamk) ? c.ksplit : c.nslots;
     return W4A8_OK;
 }
@@ -431,7 +433,7 @@ static int moe_forward_common(const uint8_t* x_e4m3, const float* a1_scale, int 
     if (int st = current_device(&sms))
         return st;
     MoeWs w;
-    moe_ws(T, H, I, k, &w, ws, dynamic);
+    moe_ws(T, H, I, E, k, &w, ws, dynamic);
     MoeLaunch L{};
     L.xq = x_e4m3;
     L.a1 = a1_scale;
@@ -459,6 +461,7 @@ static int moe_forward_common(const uint8_t* x_e4m3, const float* a1_scale, int 
     L.s0h = w.s0h;
     L.ypart = w.ypart;
     L.done = w.done;
+    L.wq8 = w.wq8;
     // header words 48 and 49: the one-launch forward's claim counters, zero
     // when the workspace is allocated and left zero by every call
     L.claim = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + 192);
@@ -488,9 +491,8 @@ int moe_w4a8_forward(const uint8_t* x_e4m3, const float* a1_scale, int T, int H,
 
 size_t moe_w4a8_dynamic_workspace_size(int T, int H, int I, int E, int k)
 {
-    (void)E;
     MoeWs w;
-    return moe_ws(T, H, I, k, &w, nullptr, true);
+    return moe_ws(T, H, I, E, k, &w, nullptr, true);
 }
 
 int moe_w4a8_forward_dynamic(const uint8_t* x_e4m3, const float* a1_scale, int T, int H, int I, int E, int k,

@@ -65,7 +65,12 @@ struct MoeConfig {
     int streamk;   // 1: the down GEMM takes equal K-block ranges per CTA
     int nslots;    // stream-K partial slots per output
     int fused;     // 1: gate_up and down run in one launch (K split ksplit ways)
+    int a8;        // 1: the weights are unpacked once per call (moe_upcast_kernel) and
+                   //    the GEMMs load them by TMA (prefill-sized calls)
 };
+// Whether calls of T tokens unpack the weights once per call (and need room
+// for the unpacked weights in the workspace).
+bool moe_unpack_once(int T);
 // one_launch: whether the caller's path allows both projections in one
 // launch (not with the dynamic intermediate scale, which needs max|h| first)
 MoeConfig moe_pick_config(int T, int H, int I, int E, int k, int num_sms, bool one_launch);
@@ -79,6 +84,7 @@ struct MoeLaunch {
     uint16_t* out;
     // workspace pieces
     uint8_t* xp; long long* s0x; uint8_t* hq; unsigned long long* s0h; float* ypart;
+    uint8_t* wq8;  // unpacked weights [E, 2I, H] (gate_up, tile row order) then [E, H, I]
     int* done;  // [E] per-expert gate_up progress of the one-launch forward
     int* claim; // [2] its tile-claim counters (zero between calls)
     // dynamic intermediate scale (moe_w4a8_forward_dynamic): h in fp32, its

@@ -7,7 +7,7 @@
 // node", Motivation: INT4 weights lower the memory bandwidth of decoding, the
 // FP8 tensor cores do the math.
 //
-// Grouped GEMM design (one persistent CTA per SM, 8 + NCONV warps):
+// Grouped GEMM design (one persistent CTA per SM, 4 + NCONV + NEPI warps):
 //   warp 0      TMA producer of the packed INT4 weight tiles [128 rows x KC/2
 //               bytes] into the W ring (starts before the dependency wait).
 //   warp 2      TMA producer of the expert's activation tiles [BN x KC] into
@@ -17,8 +17,9 @@
 //   warps 4..   converters: thread r owns A row r; it turns its packed nibbles
 //               into E4M3 bytes, in TMEM (tcgen05.st) for token tiles up to 128,
 //               else in the 128-byte-swizzled K-major shared-memory layout.
-//   last 4      epilogue: tcgen05.ld of the fp32 accumulators (lane = weight
-//               row, column = token), scales, activation, stores.
+//   last NEPI   epilogue: tcgen05.ld of the fp32 accumulators (lane = weight
+//               row, column = token), scales, activation, stores; with 8 warps
+//               the two warps of a lane quadrant take alternate 32-column chunks.
 // The MMA runs "swapped": M = 128 weight rows, N = the expert's tokens, so a
 // decode step with a handful of tokens per expert still uses M = 128 and the
 // weights stream through the SMs once.
@@ -77,7 +78,7 @@ struct MoeGemmParams {
     uint32_t* err;
 };
 
-template <int MODE, int BN, int KC, int NW, int NX, int NXT, int NCONV, int NISS>
+template <int MODE, int BN, int KC, int NW, int NX, int NXT, int NCONV, int NISS, int NB, int NEPI>
 struct MoeTraits {
     static constexpr int kAtoms = KC / 128;                      // 128-byte K atoms of A and B
     static constexpr int kWBytes = 128 * KC / 2;                 // packed weights per stage
@@ -88,12 +89,19 @@ struct MoeTraits {
     static constexpr int kASlot = kAtoms * 128 * 128;            // unpacked A of a shared-memory slot
     static constexpr int kACols = KC / 4;                        // unpacked A of a TMEM slot
     // X slots 0..NXT-1 keep their unpacked A in TMEM, slots NXT..NX-1 in
-    // shared memory (after the B tiles)
-    static constexpr int kData = NW * kWBytes + NX * kXBytes + (NX - NXT) * kASlot;
-    static constexpr int kBars = 2 * NW + 3 * NX + 4 + 2 + 2 * kTileQ;   // + drain, tile queue
+    // shared memory (after the B tiles). With NB != NX the activation tiles
+    // have a ring of their own (NB slots), decoupled from the A slots: the
+    // activation copies then run NB stages ahead instead of NX.
+    static constexpr bool kSplitB = (NB != NX);
+    // No converter warps (NCONV = 0): A arrives by TMA from weights unpacked
+    // ahead of the GEMM (moe_upcast_kernel) into the shared-memory A slots,
+    // loaded by warp 0 in place of the packed weight stream (no W ring).
+    static constexpr bool kA8 = (NCONV == 0);
+    static constexpr int kData = NW * kWBytes + NB * kXBytes + (NX - NXT) * kASlot;
+    static constexpr int kBars = 2 * NW + 2 * NB + 2 * NX + 4 + 2 + 2 * kTileQ;   // + drain, tile queue
     static constexpr int kCtrl = kBars * 8 + 16 + 4 * (256 + 260 + 260 + 260 + kTileQ);
     // MODE 3 tile queue: every role but the weight producer frees each entry
-    static constexpr int kTileReaders = 1 + NISS + NCONV + 4;
+    static constexpr int kTileReaders = 1 + NISS + NCONV + NEPI;
     static constexpr int kSmem = 1024 + kData + kCtrl;
     // two accumulator buffers (tile i / tile i+1), each with one partial sum
     // per MMA-issuing thread
@@ -101,9 +109,9 @@ struct MoeTraits {
     static constexpr int kTmemNeed = kDCols + NXT * kACols;
     static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
                                    : kTmemNeed <= 256 ? 256 : 512;
-    static constexpr int kThreads = 32 * (8 + NCONV);
+    static constexpr int kThreads = 32 * (4 + NCONV + NEPI);
     static constexpr int kEpi0 = 4 + NCONV;                      // first epilogue warp
-    static constexpr int kPar = NCONV / 4;                       // converter warps per quadrant
+    static constexpr int kPar = NCONV >= 4 ? NCONV / 4 : 1;     // converter warps per quadrant
     static_assert(kWBytes % 1024 == 0 && kXBytes % 1024 == 0 && kASlot % 1024 == 0, "stage alignment");
     static_assert(NXT >= 0 && NXT <= NX, "TMEM A slots");
     // where X slot x keeps its unpacked A; a compile-time constant unless the
@@ -120,7 +128,9 @@ struct MoeTraits {
     static_assert(kSmem <= 232448, "shared memory budget");
     static_assert(kTmemNeed <= 512, "tensor memory budget");
     static_assert(BN % 16 == 0 && BN <= 256, "token tile");
-    static_assert(NCONV % 4 == 0 && NCONV >= 4, "converters cover the four TMEM lane quadrants");
+    static_assert((NCONV % 4 == 0 && NCONV >= 4) || (kA8 && NW == 0 && NXT == 0 && !kSplitB),
+                  "converters cover the four TMEM lane quadrants; without them A comes by TMA into shared memory");
+    static_assert(NEPI == 4 || NEPI == 8, "epilogue warps: one or two per TMEM lane quadrant");
     // Converter warp w takes the stages g with g % kPar == (w - 4) / 4 and waits
     // on the rings' barriers by phase parity. A parity wait cannot tell phase r
     // from r + 2, so every warp must see every round of each slot it serves:
@@ -130,6 +140,10 @@ struct MoeTraits {
     // MMA issuer i takes the stages g with g % NISS == i and waits on afull by
     // parity as well, so the X ring depth must be a multiple of NISS.
     static_assert((NISS == 1 || NISS == 2) && NX % NISS == 0, "MMA issuers");
+    // a separate activation ring is waited on by the issuers (by parity) and
+    // holds only activation tiles: its depth is a multiple of the issuers, and
+    // every A slot lives in tensor memory
+    static_assert(!kSplitB || (NB % NISS == 0 && NB > 0 && NXT == NX), "activation ring");
 };
 
 struct TileInfo {
@@ -246,26 +260,32 @@ __device__ __forceinline__ float act_fn(float z, int act)
 // which both guarantees its A slot is free (bfull round r follows xfree round
 // r-1) and lets the MMA wait on afull alone: one wait and one commit per stage
 // in the single MMA thread.
-template <int MODE, int BN, int KC, int NW, int NX, int NXT, int NCONV, int NISS>
-__global__ void __launch_bounds__(32 * (8 + NCONV), 1)
+// With a separate activation ring (NB != NX; the unpacked weights all in
+// TMEM): activation tile b = g % NB arrives on bfull[b] and is freed by the
+// MMA's commit to bfree[b]; A slot x = g % NX is freed by its commit to
+// xfree[x], which the converters wait on; the MMA waits on afull[x] and
+// bfull[b].
+template <int MODE, int BN, int KC, int NW, int NX, int NXT, int NCONV, int NISS, int NB, int NEPI>
+__global__ void __launch_bounds__(32 * (4 + NCONV + NEPI), 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_b2,
                     const MoeGemmParams p)
 {
-    using Tr = MoeTraits<MODE, BN, KC, NW, NX, NXT, NCONV, NISS>;
+    using Tr = MoeTraits<MODE, BN, KC, NW, NX, NXT, NCONV, NISS, NB, NEPI>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
     uint8_t* wring = smem;
     uint8_t* xring = smem + NW * Tr::kWBytes;
-    uint8_t* aring = xring + NX * Tr::kXBytes;       // unpacked A of X slots NXT..NX-1
+    uint8_t* aring = xring + NB * Tr::kXBytes;       // unpacked A of X slots NXT..NX-1
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Tr::kData);
     uint64_t* wfull = bars;
     uint64_t* wfree = wfull + NW;
-    uint64_t* bfull = wfree + NW;
-    uint64_t* afull = bfull + NX;
+    uint64_t* bfull = wfree + NW;                   // NB entries
+    uint64_t* afull = bfull + NB;
     uint64_t* xfree = afull + NX;
-    uint64_t* accfull = xfree + NX;
+    uint64_t* bfree = xfree + NX;                   // NB entries (separate activation ring only)
+    uint64_t* accfull = bfree + NB;
     uint64_t* accempty = accfull + 2;
     uint64_t* drain = accempty + 2;                 // one per MMA issuer
     uint64_t* tq_full = drain + 2;                  // MODE 3 tile queue
@@ -287,13 +307,16 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
             mbar_init(smem_u32(&wfree[i]), 4);   // one converter warp per lane quadrant
         }
         for (int i = 0; i < NX; ++i) {
-            mbar_init(smem_u32(&bfull[i]), 1);
-            mbar_init(smem_u32(&afull[i]), 4);
+            mbar_init(smem_u32(&afull[i]), Tr::kA8 ? 1 : 4);   // TMA of A, or one converter warp per quadrant
             mbar_init(smem_u32(&xfree[i]), 1);
+        }
+        for (int i = 0; i < NB; ++i) {
+            mbar_init(smem_u32(&bfull[i]), 1);
+            mbar_init(smem_u32(&bfree[i]), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&accfull[i]), NISS);
-            mbar_init(smem_u32(&accempty[i]), 4);
+            mbar_init(smem_u32(&accempty[i]), NEPI);
         }
         mbar_init(smem_u32(&drain[0]), 1);
         mbar_init(smem_u32(&drain[1]), 1);
@@ -373,9 +396,10 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                 grid_dep_wait();
                 grid_dep_launch();
             }
-            const int nslot = wprod ? NW : NX;
-            uint64_t* fullb = wprod ? wfull : bfull;
-            uint64_t* freeb = wprod ? wfree : xfree;
+            // warp 0 fills the W ring, or (no converters) the A slots of the X ring
+            const int nslot = wprod ? (Tr::kA8 ? NX : NW) : NB;
+            uint64_t* fullb = wprod ? (Tr::kA8 ? afull : wfull) : bfull;
+            uint64_t* freeb = wprod ? (Tr::kA8 ? xfree : wfree) : (Tr::kSplitB ? bfree : xfree);
             const uint64_t pol = wprod ? policy_evict_first() : policy_evict_last();
             int s = 0;
             uint32_t ph = 0;
@@ -395,9 +419,9 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                 const CUtensorMap* mb = second ? &tm_b2 : &tm_b;
                 if constexpr (MODE == 3) {
                     // the down tile reads the intermediate of expert e (TMA): wait
-                    // until the 4 epilogue warps of each of e's gate_up tiles counted
+                    // until the NEPI epilogue warps of each of e's gate_up tiles counted
                     if (!wprod && second && ti.e > seen) {
-                        const int need = 4 * (s_pre[ti.e + 1] - s_pre[ti.e]);
+                        const int need = NEPI * (s_pre[ti.e + 1] - s_pre[ti.e]);
                         if (!counter_wait_or_abort(p.done + ti.e, need, s_abort)) {
                             ok = false;
                             break;
@@ -414,7 +438,15 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                     }
                     const uint32_t fb = smem_u32(&fullb[s]);
                     const int kel = (ti.ks * kbl + kb) * KC;  // first K element
-                    if (wprod) {
+                    if (Tr::kA8 && wprod) {
+                        // unpacked weight rows, already in the tile's row order
+                        mbar_arrive_expect_tx(fb, Tr::kASlot);
+                        uint8_t* st = aring + (s - NXT) * Tr::kASlot;
+                        const int r0 = ti.e * rpe + ti.rt * 128;
+#pragma unroll
+                        for (int a = 0; a < Tr::kAtoms; ++a)
+                            tma_load_2d_hint(smem_u32(st + a * 128 * 128), mw, kel + a * 128, r0, fb, pol);
+                    } else if (wprod) {
                         mbar_arrive_expect_tx(fb, Tr::kWBytes);
                         uint8_t* st = wring + s * Tr::kWBytes;
 #pragma unroll
@@ -478,8 +510,8 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
         // (few-token) tiles of decoding.
         if (lane == 0) {
             const int me = (warp == 1) ? 0 : 1;
-            int x = 0;
-            uint32_t ph = 0;
+            int x = 0, b = 0;
+            uint32_t ph = 0, bph = 0;
             uint32_t g = 0;
             int it = 0;
             bool ok = true;
@@ -500,12 +532,13 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                 bool first = true;
                 for (int kb = 0; kb < wi.nkb; ++kb, ++g) {
                     if (static_cast<int>(g % NISS) == me) {
-                        if (!mbar_wait_or_abort(smem_u32(&afull[x]), ph, s_abort)) {
+                        if (!mbar_wait_or_abort(smem_u32(&afull[x]), ph, s_abort) ||
+                            ((Tr::kSplitB || Tr::kA8) && !mbar_wait_or_abort(smem_u32(&bfull[b]), bph, s_abort))) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint8_t* st = xring + x * Tr::kXBytes;
+                        const uint8_t* st = xring + (Tr::kSplitB ? b : x) * Tr::kXBytes;
                         const uint64_t bd0 = desc_kmajor_sw128(smem_u32(st));
                         const bool a_tmem = Tr::a_in_tmem(x);
                         const uint64_t ad0 =
@@ -526,10 +559,16 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                         }
                         first = false;
                         umma_commit(smem_u32(&xfree[x]));
+                        if constexpr (Tr::kSplitB)
+                            umma_commit(smem_u32(&bfree[b]));
                     }
                     if (++x == NX) {
                         x = 0;
                         ph ^= 1u;
+                    }
+                    if (++b == NB) {
+                        b = 0;
+                        bph ^= 1u;
                     }
                 }
                 if (!ok)
@@ -562,8 +601,12 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
             const int src = tile_is_gate_up<MODE>(wi.t, n_gu) ? src_gu : r;
             for (int kb = 0; kb < wi.nkb; ++kb, ++g) {
                 if (static_cast<int>(g % Tr::kPar) == par) {
+                    // the A slot is free once the MMAs of its previous round
+                    // completed: seen through that round's activation copy
+                    // (shared ring), or the MMA's commit (separate ring)
                     if (!mbar_wait_or_abort(smem_u32(&wfull[w]), wph, s_abort) ||
-                        !mbar_wait_or_abort(smem_u32(&bfull[x]), xph, s_abort)) {
+                        !mbar_wait_or_abort(smem_u32(Tr::kSplitB ? &xfree[x] : &bfull[x]),
+                                            Tr::kSplitB ? (xph ^ 1u) : xph, s_abort)) {
                         ok = false;
                         break;
                     }
@@ -628,6 +671,8 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
     } else if (warp >= Tr::kEpi0) {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;
+        const int sub = (warp - Tr::kEpi0) >> 2;   // chunk phase: 32-column chunks sub, sub + NEPI/4, ...
+        constexpr int kChStep = NEPI / 4;
         grid_dep_wait();
         grid_dep_launch();
         const float a1 = __ldg(p.a1);
@@ -677,7 +722,7 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                 const int i = ti.rt * 64 + 16 * q + (lane & 15);
                 const float sg = a1 * __ldg(p.s_gu + static_cast<int64_t>(ti.e) * 2 * p.I + i);
                 const float su = a1 * __ldg(p.s_gu + static_cast<int64_t>(ti.e) * 2 * p.I + p.I + i);
-                for (int ch = 0; ch < nchunks; ++ch) {
+                for (int ch = sub; ch < nchunks; ch += kChStep) {
                     // lane l fetches the exact shift of column ch*32 + l up front
                     // (the loop below hands it around by shuffle), so no load
                     // waits behind the byte stores of the loop
@@ -686,7 +731,7 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                     uint32_t v[32];
                     load_acc(ch * 32, v);
                     const float my_shift = static_cast<float>(my_s0x) * (1.0f / 64.0f);
-                    int s512[16];
+                    float s512[16];   // 512 * dec(hq): integers, summed exactly in fp32
                     float hmax_l = 0.0f;
 #pragma unroll
                     for (int cc = 0; cc < 16; ++cc) {
@@ -697,7 +742,7 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                         const float pu = half ? __uint_as_float(v[cc + 16]) : recv;
                         const int col = ch * 32 + cc + 16 * half;
                         const float shift = __shfl_sync(0xFFFFFFFFu, my_shift, cc + 16 * half);
-                        s512[cc] = 0;
+                        s512[cc] = 0.0f;
                         if (col < ti.ntok) {
                             const int pos = ti.tok0 + col;
                             const float G = fmaf(512.0f, pg, -shift);
@@ -710,7 +755,7 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                                 // hq = E4M3(h / a2): IEEE division, then one RNE rounding
                                 const uint32_t code = cvt_e4m3(__fdiv_rn(h, a2));
                                 p.hq[static_cast<int64_t>(pos) * p.I + kperm(i)] = static_cast<uint8_t>(code);
-                                s512[cc] = e4m3_times512(code);
+                                s512[cc] = e4m3_times512_f32(code);
                             }
                         }
                     }
@@ -728,13 +773,14 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                             const bool upper = (lane & m) != 0;
 #pragma unroll
                             for (int x = 0; x < m; ++x) {
-                                const int send = upper ? s512[x] : s512[x + m];
-                                const int recv = __shfl_xor_sync(0xFFFFFFFFu, send, m);
+                                const float send = upper ? s512[x] : s512[x + m];
+                                const float recv = __shfl_xor_sync(0xFFFFFFFFu, send, m);
                                 s512[x] = (upper ? s512[x + m] : s512[x]) + recv;
                             }
                         }
+                        // |sum| <= 16 * 229376 < 2^24: exact, and exactly an integer
                         const int col = ch * 32 + lane;
-                        if (col < ti.ntok && s512[0] != 0)
+                        if (col < ti.ntok && s512[0] != 0.0f)
                             atomicAdd(p.s0h + ti.tok0 + col,
                                       static_cast<unsigned long long>(static_cast<long long>(s512[0])));
                     }
@@ -759,13 +805,13 @@ __global__ void __launch_bounds__(32 * (8 + NCONV), 1)
                     slot = -1;
                 }
                 float* yb = p.ypart + (static_cast<int64_t>(slot) * p.A + ti.tok0) * p.H + n;
-                if (p.streamk && wi.last) {
+                if (p.streamk && wi.last && sub == 0) {
                     // the tile's last segment: slots no CTA writes hold zero
                     for (int sl = wi.slot + 1; sl < p.nslots; ++sl)
                         for (int col = 0; col < ti.ntok; ++col)
                             p.ypart[(static_cast<int64_t>(sl) * p.A + ti.tok0 + col) * p.H + n] = 0.0f;
                 }
-                for (int ch = 0; ch < nchunks; ++ch) {
+                for (int ch = sub; ch < nchunks; ch += kChStep) {
                     uint32_t v[32];
                     load_acc(ch * 32, v);
 #pragma unroll
@@ -848,6 +894,57 @@ __global__ void __launch_bounds__(128) moe_gather_kernel(const uint8_t* __restri
             total += red[w];
         s0x[pos] = total;
         s0h[pos] = 0ull;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Prefill: the INT4 weights of every expert with tokens, unpacked once per call
+// into the E4M3 operand bytes the GEMM's converters produce (value
+// (q + 8) * 2^-9, codes of a packed word in the order of unpack8), so that the
+// GEMM loads A by TMA and its tiles each reuse it instead of unpacking it again
+// for every token tile. gate_up rows are stored in tile order: 128-row tile rt
+// holds, for each TMEM lane quadrant q, gate rows rt*64 + 16q + 0..15 and then
+// the matching up rows (the pairing of the gated epilogue). One thread per 16
+// packed bytes (32 weights) of a row.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) moe_upcast_kernel(const int32_t* __restrict__ w_gu,
+                                                         const int32_t* __restrict__ w_d, int E, int H, int I,
+                                                         const int32_t* __restrict__ counts,
+                                                         uint8_t* __restrict__ a_gu, uint8_t* __restrict__ a_d)
+{
+    grid_dep_wait();
+    grid_dep_launch();
+    const int64_t gu_chunks = static_cast<int64_t>(E) * 2 * I * (H / 32);   // 16-byte chunks of packed gate_up
+    const int64_t d_chunks = static_cast<int64_t>(E) * H * (I / 32);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < gu_chunks + d_chunks;
+         c += stride) {
+        const bool gu = c < gu_chunks;
+        const int64_t cc = gu ? c : c - gu_chunks;
+        const int K = gu ? H : I;
+        const int rows = gu ? 2 * I : H;
+        const int per_row = K / 32;
+        const int64_t row = cc / per_row;             // expert * rows + output row
+        const int j = static_cast<int>(cc - row * per_row);
+        const int e = static_cast<int>(row / rows);
+        if (__ldg(counts + e) == 0)
+            continue;
+        const int R = static_cast<int>(row - static_cast<int64_t>(e) * rows);
+        int src = R;
+        if (gu) {
+            const int rt = R >> 7, r = R & 127, q = r >> 5, l = r & 31;
+            src = (l < 16) ? rt * 64 + 16 * q + l : I + rt * 64 + 16 * q + (l - 16);
+        }
+        const int32_t* w = gu ? w_gu : w_d;
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(w + (static_cast<int64_t>(e) * rows + src) * (K / 8)) + j);
+        uint32_t o[8];
+        unpack8(v.x, o[0], o[1]);
+        unpack8(v.y, o[2], o[3]);
+        unpack8(v.z, o[4], o[5]);
+        unpack8(v.w, o[6], o[7]);
+        uint4* dst = reinterpret_cast<uint4*>((gu ? a_gu : a_d) + row * K) + 2 * j;
+        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
     }
 }
 
@@ -1066,12 +1163,15 @@ static int fused_ksplit(int T, int H, int I, int E, int k, int bn, int kc, int n
     return best;
 }
 
+bool moe_unpack_once(int T) { return T > 128; }
+
 MoeConfig moe_pick_config(int T, int H, int I, int E, int k, int num_sms, bool one_launch)
 {
     MoeConfig c;
     c.bn = pick_bn(T);
     c.kc = (c.bn <= 128) ? 256 : 128;
     c.fused = 0;
+    c.a8 = moe_unpack_once(T) ? 1 : 0;
     if (one_launch && c.kc == 256) {
         c.fused = 1;
         c.ksplit = fused_ksplit(T, H, I, E, k, c.bn, c.kc, num_sms);
@@ -1122,12 +1222,12 @@ MoeConfig moe_pick_config(int T, int H, int I, int E, int k, int num_sms, bool o
     return c;
 }
 
-template <int MODE, int BN, int KC, int NW, int NX, int NXT, int NCONV, int NISS>
+template <int MODE, int BN, int KC, int NW, int NX, int NXT, int NCONV, int NISS, int NB = NX, int NEPI = 4>
 static int launch_gemm(const CUtensorMap& tw, const CUtensorMap& tb, const CUtensorMap& tw2, const CUtensorMap& tb2,
                        const MoeGemmParams& prm, int grid, cudaStream_t s)
 {
-    using Tr = MoeTraits<MODE, BN, KC, NW, NX, NXT, NCONV, NISS>;
-    auto kern = moe_gemm_kernel<MODE, BN, KC, NW, NX, NXT, NCONV, NISS>;
+    using Tr = MoeTraits<MODE, BN, KC, NW, NX, NXT, NCONV, NISS, NB, NEPI>;
+    auto kern = moe_gemm_kernel<MODE, BN, KC, NW, NX, NXT, NCONV, NISS, NB, NEPI>;
     // attribute set on every launch: cheap, and correct for every device
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Tr::kSmem) != cudaSuccess)
         return kErrLaunch;
@@ -1136,11 +1236,18 @@ static int launch_gemm(const CUtensorMap& tw, const CUtensorMap& tb, const CUten
                : kErrLaunch;
 }
 
-// Token tile -> pipeline shape. Up to 128 tokens the unpacked weights live in
-// tensor memory, which leaves shared memory to a deep TMA ring (192 KB); the
-// 256-token tile needs all of TMEM for its two accumulators and keeps A in
-// shared memory.
-// MODE 3 (both projections in one launch) exists for the TMEM-A shapes only.
+// Token tile -> pipeline shape. Up to 128 tokens (decode) the weights are
+// unpacked inside the GEMM into tensor memory, which leaves shared memory to a
+// deep TMA ring: A and the activation tile share one ring of K = 256 stages.
+// Above (prefill) each weight tile meets many token tiles: the weights are
+// unpacked once per call by moe_upcast_kernel and the GEMM runs 256-token
+// tiles (two fp32 accumulators of 256 columns fill the 512 TMEM columns) with
+// A and the activations both loaded by TMA into shared memory, 128-wide
+// stages, 4 deep, and eight epilogue warps. (Measured on the Grok-1 prefill
+// layer: with the unpack inside the GEMM, each weight tile was unpacked again
+// for every token tile -- about 43 times at 192-token tiles -- and the
+// converter and gated-epilogue warps, not the tensor pipe, set the pace.)
+// MODE 3 (both projections in one launch) exists for the decode shapes only.
 template <int MODE>
 static int dispatch_gemm(const MoeConfig& cfg, const CUtensorMap& tw, const CUtensorMap& tb, const CUtensorMap& tw2,
                          const CUtensorMap& tb2, const MoeGemmParams& prm, int grid, cudaStream_t s)
@@ -1153,7 +1260,7 @@ static int dispatch_gemm(const MoeConfig& cfg, const CUtensorMap& tw, const CUte
         if constexpr (MODE == 3)
             return kErrLaunch;
         else
-            return launch_gemm<MODE, 256, 128, 8, 3, 0, 4, 1>(tw, tb, tw2, tb2, prm, grid, s);
+            return launch_gemm<MODE, 256, 128, 0, 4, 0, 0, 1, 4, 8>(tw, tb, tw2, tb2, prm, grid, s);
     }
 }
 
@@ -1161,6 +1268,12 @@ int launch_moe_forward(const MoeLaunch& L, const MoeConfig& cfg, int num_sms, cu
 {
     const int A = L.T * L.k;
     const int BN = cfg.bn, KC = cfg.kc;
+    const bool a8 = cfg.a8 != 0;
+    // prefill: the weights of the experts with tokens, unpacked once
+    if (a8 && launch_dependent(moe_upcast_kernel, dim3(static_cast<unsigned>(num_sms * 8)), dim3(256), 0, s,
+                               L.w_gu, L.w_d, L.E, L.H, L.I, L.counts, L.wq8, L.wq8 + static_cast<int64_t>(L.E) * 2 *
+                                                                                        L.I * L.H) != cudaSuccess)
+        return kErrLaunch;
     // activations: gather + exact per-token sums
     const bool fused = cfg.fused && !L.dynamic;
     if (launch_dependent(moe_gather_kernel, dim3(A), dim3(128), 0, s, L.xq, L.H, L.k, L.sorted_ids, A, L.xp,
@@ -1171,12 +1284,23 @@ int launch_moe_forward(const MoeLaunch& L, const MoeConfig& cfg, int num_sms, cu
     const CUtensorMapSwizzle wsw = (KC == 128) ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
     const uint32_t wbox = (KC == 128) ? 64u : 128u;
     CUtensorMap tw_gu, tb_gu, tw_d, tb_d;
-    if (!encode_map_2d(&tw_gu, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.w_gu, L.H / 2,
-                       static_cast<uint64_t>(L.E) * 2 * L.I, L.H / 2, wbox, 64, wsw) ||
-        !encode_map_2d(&tb_gu, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.xp, L.H, A, L.H, 128, BN,
+    const uint8_t* wq8_d = a8 ? L.wq8 + static_cast<int64_t>(L.E) * 2 * L.I * L.H : nullptr;
+    if (a8) {
+        // unpacked weights: rows of E4M3 bytes, 128 x 128 boxes, 128-byte swizzle
+        if (!encode_map_2d(&tw_gu, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.wq8, L.H, static_cast<uint64_t>(L.E) * 2 * L.I,
+                           L.H, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_map_2d(&tw_d, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq8_d, L.I, static_cast<uint64_t>(L.E) * L.H, L.I,
+                           128, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+            return kErrLaunch;
+    } else if (!encode_map_2d(&tw_gu, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.w_gu, L.H / 2,
+                              static_cast<uint64_t>(L.E) * 2 * L.I, L.H / 2, wbox, 64, wsw) ||
+               !encode_map_2d(&tw_d, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.w_d, L.I / 2,
+                              static_cast<uint64_t>(L.E) * L.H, L.I / 2, wbox, 128, wsw)) {
+        return kErrLaunch;
+    }
+    if (
+!encode_map_2d(&tb_gu, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.xp, L.H, A, L.H, 128, BN,
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_map_2d(&tw_d, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.w_d, L.I / 2,
-                       static_cast<uint64_t>(L.E) * L.H, L.I / 2, wbox, 128, wsw) ||
         !encode_map_2d(&tb_d, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.hq, L.I, A, L.I, 128, BN,
                        CU_TENSOR_MAP_SWIZZLE_128B))
         return kErrLaunch;

@@ -320,6 +320,20 @@ __device__ __forceinline__ int e4m3_times512(uint32_t c)
     const int mag = e ? ((8 + m) << (e - 1)) : m;
     return (c & 0x80u) ? -mag : mag;
 }
+// The same as an fp32 number: the hardware E4M3 -> f16 conversion is exact
+// for every finite code, and 512 * value is an integer below 2^18, so sums of
+// up to 64 of them stay exact in fp32.
+__device__ __forceinline__ float e4m3_times512_f32(uint32_t c)
+{
+    float r;
+    asm("{\n\t.reg .b32 t;\n\t.reg .b16 lo, hi;\n\t"
+        "cvt.rn.f16x2.e4m3x2 t, %1;\n\t"
+        "mov.b32 {lo, hi}, t;\n\t"
+        "cvt.f32.f16 %0, lo;\n\t}"
+        : "=f"(r)
+        : "h"(static_cast<uint16_t>(c & 0xFFu)));
+    return r * 512.0f;
+}
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b)
 {
     return __uint_as_float(static_cast<uint32_t>(b) << 16);
