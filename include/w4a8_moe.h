@@ -163,7 +163,7 @@ size_t moe_route_gate_workspace_size(int T, int H, int E, int k);
  *   w_d  [E, H, I/8] i32 and s_d [E, H] fp32.
  *   topk_ids, topk_w, counts, offsets, sorted_ids, inv_perm: from moe_route.
  *   out_bf16 [T, H] bf16: out.
- *   Requires H and I positive multiples of 256, 1 <= k <= E <= 256, T >= 1.
+ *   Requires H and I positive multiples of 128, 1 <= k <= E <= 256, T >= 1.
  *   ws: moe_w4a8_workspace_size(T, H, I, E, k) bytes. Above 128 tokens this
  *       includes E * 3 * I * H bytes where the call unpacks the INT4 weights of
  *       the experts with tokens once (to E4M3 operand bytes) before the GEMMs.

@@ -123,8 +123,9 @@ def test_forward_shape_rules(lib):
     ws = lib.moe_w4a8_workspace_size(32, 4096, 14336, 8, 2)
     args = lambda T, H, I, E, k, act=0: [g, g, T, H, I, E, k, g, g, g, g, g, act, g, g, g, g, g, g, g,
                                          g, ws, None]
-    assert f(*args(32, 4096 + 128, 14336, 8, 2)) == 2      # H not a multiple of 256
-    assert f(*args(32, 4096, 14336 + 128, 8, 2)) == 2      # I not a multiple of 256
+    assert f(*args(32, 4096 + 64, 14336, 8, 2)) == 2       # H not a multiple of 128
+    assert f(*args(32, 4096, 14336 + 64, 8, 2)) == 2       # I not a multiple of 128
+    assert f(*args(32, 0, 14336, 8, 2)) == 2
     assert f(*args(32, 4096, 14336, 8, 3, act=2)) == 2     # unknown activation
     assert f(*args(32, 4096, 14336, 2, 3)) == 2            # k > E
     bad = args(32, 4096, 14336, 8, 2)
@@ -180,7 +181,8 @@ def test_plan_of_the_decode_and_prefill_layers(lib):
 
 
 def test_plan_rejects_what_the_forward_rejects(lib):
-    assert _plan(lib, 32, 4096 + 128, 14336, 8, 2)[0] == 2
+    assert _plan(lib, 32, 4096 + 64, 14336, 8, 2)[0] == 2
+    assert _plan(lib, 32, 4096 + 128, 14336 + 128, 8, 2)[0] == 0   # multiples of 128 are accepted
     assert _plan(lib, 0, 4096, 14336, 8, 2)[0] == 2
     assert _plan(lib, 32, 4096, 14336, 8, 2, sms=0)[0] == 2
     f = lib.moe_w4a8_plan
@@ -195,12 +197,12 @@ def test_plan_fits_the_workspace(lib):
     lib.moe_w4a8_workspace_size.restype = ctypes.c_size_t
     for T in (1, 2, 3, 5, 8, 16, 31, 32, 33, 64, 100, 128, 129, 300, 1024):
         for (H, I, E, k) in ((4096, 14336, 8, 2), (6144, 32768, 8, 2), (256, 512, 16, 4), (2048, 1536, 64, 6),
-                             (512, 256, 256, 8)):
+                             (512, 256, 256, 8), (384, 640, 8, 2), (128, 128, 4, 1), (640, 384, 16, 4)):
             for dyn in (0, 1):
                 for sms in (152, 148, 7):
                     st, p = _plan(lib, T, H, I, E, k, dyn, sms)
                     assert st == 0
-                    kb = I // p[1]
+                    kb = -(-I // p[1])          # stages of the down K, the last one possibly partial
                     assert kb % p[2] == 0 and kb // p[2] >= 2 or p[2] == 1
                     ws = lib.moe_w4a8_workspace_size(T, H, I, E, k)
                     assert ws >= p[7] * T * k * H * 4, (T, H, I, E, k, dyn, sms, p)

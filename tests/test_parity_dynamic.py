@@ -19,6 +19,7 @@ pytestmark = pytest.mark.gpu
     (16, 256, 512, 8, 2, 0, 0.0),        # tiny
     (33, 256, 256, 8, 2, 1, 0.0),        # ragged, GELU
     (32, 4096, 14336, 8, 2, 0, 0.5),     # Mixtral-8x7B decode
+    (200, 384, 640, 8, 2, 1, 0.0),       # prefill plan (weights unpacked once), ragged K stages
 ])
 def test_dynamic_scale_forward(T, H, I, E, k, act, bias):
     ensure_built()

@@ -43,6 +43,12 @@ def test_tiny_layer_all_tokens():
     (7, 256, 256, 1, 1, 0),       # E = 1, k = 1: dense W4A8 MLP
     (64, 768, 512, 16, 4, 1),     # k = 4, 16 experts, H not a power of two
     (64, 256, 256, 256, 8, 0),    # the most experts the boundary accepts, top-8
+    (5, 128, 128, 4, 2, 0),       # the smallest H and I: one half-filled K stage
+    (24, 384, 640, 8, 2, 1),      # H, I = 128 mod 256: a ragged last K stage in both GEMMs
+    (40, 640, 384, 8, 2, 0),      # the same, 64-token tile
+    (100, 384, 384, 8, 2, 1),     # the same, 128-token tile
+    (3, 640, 640, 8, 2, 0),       # the same, stream-K down projection (T*k <= E)
+    (150, 384, 640, 8, 2, 0),     # prefill plan (256-token tiles, weights unpacked once), K = 128 stages
 ])
 def test_shapes_and_tails(T, H, I, E, k, act):
     case = MoECase(T, H, I, E, k, act, seed=T + E)

@@ -165,7 +165,7 @@ static size_t moe_ws(int T, int H, int I, int E, int k, MoeWs* w, void* ws, bool
 // Shapes the MoE forward accepts (see the header).
 static bool moe_shape_ok(int T, int H, int I, int E, int k)
 {
-    return T >= 1 && H >= 256 && H % 256 == 0 && I >= 256 && I % 256 == 0 && E >= 1 && E <= 256 && k >= 1 &&
+    return T >= 1 && H >= 128 && H % 128 == 0 && I >= 128 && I % 128 == 0 && E >= 1 && E <= 256 && k >= 1 &&
            k <= E && static_cast<int64_t>(T) * k < (static_cast<int64_t>(1) << 30) &&
            static_cast<int64_t>(E) * 2 * I < (static_cast<int64_t>(1) << 31);
 }

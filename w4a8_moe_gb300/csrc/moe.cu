@@ -30,6 +30,12 @@
 // then the down tiles, and a down tile of expert e waits on a per-expert
 // count of finished gate_up tiles, so no SM idles between the projections.
 //
+// K need not be a multiple of the stage width KC: when H or I is 128 more
+// than a multiple of 256, the last stage of a tile reaches past K, TMA fills
+// the activation (and packed weight) bytes beyond K with zeros, and those
+// activation zeros make the extra products vanish (the exact row sums below
+// cover the real K only).
+//
 // INT4 -> E4M3 upcast. A nibble n holds q = n - 16*(n >= 8). The byte
 // o = n ^ 8 = q + 8 lies in 0..15, and the E4M3 codes 0x00..0x0F encode
 // exactly o * 2^-9 (subnormals plus the first normal binade share the spacing
@@ -1134,7 +1140,7 @@ static int fused_ksplit(int T, int H, int I, int E, int k, int bn, int kc, int n
     const int64_t per = (A + act - 1) / act;
     const int64_t ntt = (per + bn - 1) / bn;
     const int64_t n_gu = act * (I / 64) * ntt;
-    const int kb_gu = H / kc, kb_all = I / kc;
+    const int kb_gu = (H + kc - 1) / kc, kb_all = (I + kc - 1) / kc;
     const int kmax = moe_ksplit_max(T, k);
     const int64_t G = num_sms;
     const double stage_bytes = static_cast<double>(G) * 128 * kc / 2;   // one stage on every SM
@@ -1182,7 +1188,7 @@ MoeConfig moe_pick_config(int T, int H, int I, int E, int k, int num_sms, bool o
     // Split the down projection's K so that its tiles fill the SMs: the cost
     // of a split d is waves(d) * (stages per tile + a fixed per-tile cost of
     // about one stage: the accumulator hand-off and the epilogue tail).
-    const int kblocks = I / c.kc;
+    const int kblocks = (I + c.kc - 1) / c.kc;
     const int base_tiles = E * (H / 128);
     const int kmax = moe_ksplit_max(T, k);
     int best = 1;
@@ -1334,12 +1340,12 @@ int launch_moe_forward(const MoeLaunch& L, const MoeConfig& cfg, int num_sms, cu
         MoeGemmParams f = g;
         f.rows_per_expert = 2 * L.I;
         f.rt_count = L.I / 64;
-        f.kblocks = L.H / KC;
+        f.kblocks = (L.H + KC - 1) / KC;
         f.ksplit = 1;
         f.rows_per_expert2 = L.H;
         f.rt_count2 = L.H / 128;
         f.ksplit2 = cfg.ksplit;
-        f.kblocks2 = L.I / KC / cfg.ksplit;
+        f.kblocks2 = (L.I + KC - 1) / KC / cfg.ksplit;
         const int64_t tiles = static_cast<int64_t>(f.rt_count + f.rt_count2 * cfg.ksplit) * tok_tiles_max;
         const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
         mark(0);
@@ -1357,7 +1363,7 @@ int launch_moe_forward(const MoeLaunch& L, const MoeConfig& cfg, int num_sms, cu
     gu.hmax = L.hmax;
     gu.rows_per_expert = 2 * L.I;
     gu.rt_count = L.I / 64;
-    gu.kblocks = L.H / KC;
+    gu.kblocks = (L.H + KC - 1) / KC;
     gu.ksplit = 1;
     int64_t tiles = static_cast<int64_t>(gu.rt_count) * tok_tiles_max;
     int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
@@ -1376,7 +1382,7 @@ int launch_moe_forward(const MoeLaunch& L, const MoeConfig& cfg, int num_sms, cu
     dn.rows_per_expert = L.H;
     dn.rt_count = L.H / 128;
     dn.ksplit = cfg.streamk ? 1 : cfg.ksplit;
-    dn.kblocks = L.I / KC / dn.ksplit;
+    dn.kblocks = (L.I + KC - 1) / KC / dn.ksplit;
     dn.streamk = cfg.streamk;
     dn.nslots = cfg.nslots;
     tiles = static_cast<int64_t>(dn.rt_count) * tok_tiles_max * dn.ksplit;
