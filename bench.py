@@ -65,6 +65,9 @@ def parse(argv=None):
     ap.add_argument("--extra", action="store_true",
                     help="also measure the router gate, the dynamic intermediate scale and the "
                          "per-tensor FP8 linear (into the suite)")
+    ap.add_argument("--only", default=None,
+                    help="skip the headline layer and print only the suite entries whose workload "
+                         "name contains this text (for profiling one workload)")
     return ap.parse_args(argv)
 
 
@@ -505,7 +508,11 @@ def rotating_copies(weight_bytes, l2_bytes, at_least=4):
     return max(at_least, math.ceil(2.2 * l2_bytes / weight_bytes))
 
 
-def suite_block_fp8(lib, dev, pk, l2_bytes):
+def wanted(name, only):
+    return only is None or only in name
+
+
+def suite_block_fp8(lib, dev, pk, l2_bytes, only=None):
     """Block-FP8 dense projections: every call reads its weights from HBM
     (rotating copies totalling more than twice the L2)."""
     import torch
@@ -513,6 +520,8 @@ def suite_block_fp8(lib, dev, pk, l2_bytes):
     from w4a8_moe_gb300 import synth
     out = []
     for (N, K) in synth.BLOCK_FP8_SHAPES:
+        if not any(wanted(f"block-FP8 linear N{N} K{K} M{M}", only) for M in synth.BLOCK_FP8_M):
+            continue
         w = synth.block_fp8_inputs(1, N, K, seed=0, device=dev)["w"].float()
         blk = w.view(N // 128, 128, K // 128, 128).abs().amax(dim=(1, 3))
         wsi = torch.where(blk > 0, blk / 448.0, torch.ones_like(blk))
@@ -523,6 +532,8 @@ def suite_block_fp8(lib, dev, pk, l2_bytes):
         wl = [q.clone() for _ in range(ncopy)]
         sl = [wsi.clone() for _ in range(ncopy)]
         for M in synth.BLOCK_FP8_M:
+            if not wanted(f"block-FP8 linear N{N} K{K} M{M}", only):
+                continue
             x = synth.block_fp8_inputs(M, N, K, seed=9, device=dev)["x"]
             y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
             wsp = torch.zeros(lib.fp8_block_linear_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
@@ -552,7 +563,7 @@ def suite_block_fp8(lib, dev, pk, l2_bytes):
     return out
 
 
-def suite_extra(lib, dev, pk, l2_bytes, st_mix, mix):
+def suite_extra(lib, dev, pk, l2_bytes, st_mix, mix, only=None):
     """The rows beyond the hot path proper: per-tensor FP8 linear, router gate
     fused with routing, and the dynamic intermediate scale."""
     import torch
@@ -560,6 +571,8 @@ def suite_extra(lib, dev, pk, l2_bytes, st_mix, mix):
     from w4a8_moe_gb300 import synth
     out = []
     for (N, K) in synth.FP8_LINEAR_SHAPES:
+        if not any(wanted(f"per-tensor FP8 linear N{N} K{K} M{M}", only) for M in synth.FP8_LINEAR_M):
+            continue
         ncopy = rotating_copies(N * K, l2_bytes)
         wl, swl = [], []
         w = synth.fp8_linear_inputs(1, N, K, seed=0, device=dev)["w"]
@@ -568,6 +581,8 @@ def suite_extra(lib, dev, pk, l2_bytes, st_mix, mix):
         wl = [q.clone() for _ in range(ncopy)]
         swl = [s_.clone() for _ in range(ncopy)]
         for M in synth.FP8_LINEAR_M:
+            if not wanted(f"per-tensor FP8 linear N{N} K{K} M{M}", only):
+                continue
             x = synth.fp8_linear_inputs(M, N, K, seed=9, device=dev)["x"]
             xq, sx = lib.w4a8_quantize_act(x)
             y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
@@ -596,6 +611,8 @@ def suite_extra(lib, dev, pk, l2_bytes, st_mix, mix):
         torch.cuda.empty_cache()
 
     for (T, H, E, k) in ((32, 4096, 8, 2), (32, 6144, 8, 2)):
+        if not wanted(f"router gate + routing T{T} H{H} E{E} k{k}", only):
+            continue
         inp = synth.router_gate_inputs(T, H, E, seed=0, device=dev)
         ws_g = torch.zeros(lib.moe_route_gate_workspace_size(T, H, E, k), dtype=torch.uint8, device=dev)
         r_out, _ = lib.moe_route_gate(inp["hidden"], inp["gate"], k, ws=ws_g)
@@ -604,6 +621,8 @@ def suite_extra(lib, dev, pk, l2_bytes, st_mix, mix):
         out.append({"workload": f"router gate + routing T{T} H{H} E{E} k{k}", "us_per_call": ms * 1e3,
                     "launches": 1})
 
+    if st_mix is None or not wanted(mix.name + ", intermediate scale calibrated per call (dynamic)", only):
+        return out
     T, H, I, E, k = mix.T, mix.H, mix.I, mix.E, mix.k
     wsd = torch.zeros(lib.moe_w4a8_dynamic_workspace_size(T, H, I, E, k), dtype=torch.uint8, device=dev)
     a2d = torch.empty(1, dtype=torch.float32, device=dev)
@@ -767,10 +786,37 @@ def run_ours(args, rank, world):
         st_mix = None
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     suite += suite_block_fp8(lib, dev, pk, l2)
-    if args.extra and st_mix is not None:
+    if args.extra:
         suite += suite_extra(lib, dev, pk, l2, st_mix, mix)
     res["suite"] = suite
     return res
+
+
+def run_only(args):
+    """Only the suite entries whose workload contains args.only (one JSON line
+    each), e.g. to profile one workload under ncu."""
+    import torch
+
+    import w4a8_moe_gb300 as lib
+    from w4a8_moe_gb300 import synth
+    dev = torch.device("cuda", torch.cuda.current_device())
+    pk = peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    out = []
+    for n in ("grok_decode", "grok_decode_t8", "grok_decode_t1", "mixtral_decode"):
+        s = synth.MOE_SHAPES[n]
+        if wanted(s.name, args.only):
+            w = make_weights(s.H, s.I, s.E, 0, dev)
+            st = prepare_moe(s, 0, dev, w)
+            del w
+            torch.cuda.empty_cache()
+            out.append(suite_moe_entry(lib, s, st, max(args.steps, 50), pk))
+            del st
+            torch.cuda.empty_cache()
+    out += suite_block_fp8(lib, dev, pk, l2, args.only)
+    out += suite_extra(lib, dev, pk, l2, None, synth.MOE_SHAPES["mixtral_decode"], args.only)
+    for e in out:
+        print(json.dumps(e), flush=True)
 
 
 def main(argv=None):
@@ -787,6 +833,10 @@ def main(argv=None):
     sys.path.insert(0, ROOT)
     import __graft_entry__
     __graft_entry__.build()
+    if args.only is not None:
+        if rank == 0:
+            run_only(args)
+        return
     res = run_ours(args, rank, world)
     if rank != 0:
         return

@@ -12,13 +12,16 @@
 // NBUF TMEM partial buffers let the MMAs run up to NBUF K-blocks ahead of the
 // fold.
 //
-// Roles (12 warps): warp 0 streams the weight tiles [128 x 128] (it starts
-// before the dependency wait: no kernel of the call writes the weights), warp 2
-// the activation tiles [BN x 128] and, into a ring of their own that only the
-// epilogue releases, the BN activation scales of each K-block; warp 1 owns TMEM
-// and issues the MMAs, whose commit alone frees a weight/activation slot;
-// warps 4-11 fold (two warps per 32-lane TMEM quadrant, each half of the BN
-// token columns). Swapped operands: M = 128 weight rows, N = BN tokens.
+// Roles (4 + 4*NFW warps): warp 0 streams the weight tiles [128 x 128] (it
+// starts before the dependency wait: no kernel of the call writes the
+// weights), warp 2 the activation tiles [BN x 128] and, into a ring of their
+// own that only the epilogue releases, the BN activation scales of each
+// K-block; warps 1 and 3 own TMEM and issue the MMAs, whose commit alone frees
+// a weight/activation slot; warps 4.. fold (NFW warps per 32-lane TMEM
+// quadrant, each BN/NFW of the token columns: with more warps in flight the
+// latency of each K-block's TMEM load, scale load and barrier round trip is
+// hidden by the other warps' work). Swapped operands: M = 128 weight rows,
+// N = BN tokens.
 //
 // When K is split over several CTAs, each writes its fp32 partial and bumps a
 // per-tile counter; the CTA that completes the count sums the partials in
@@ -41,7 +44,7 @@ struct BlkParams {
     uint32_t* err;
 };
 
-template <int BN, int PST>
+template <int BN, int PST, int NFW>
 struct BlkTraits {
     static constexpr int kA = 128 * 128;                  // weight tile
     static constexpr int kB = BN * 128;                   // activation tile
@@ -59,8 +62,12 @@ struct BlkTraits {
     static constexpr int kTmemNeed = kNbuf * BN;
     static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
                                    : kTmemNeed <= 256 ? 256 : 512;
-    static constexpr int kHalf = BN / 2;
+    static constexpr int kFold = 4 * NFW;                 // fold warps
+    static constexpr int kThreads = 32 * (4 + kFold);
+    static constexpr int kHalf = BN / NFW;                // token columns per fold warp
     static constexpr int kChunk = kHalf < 32 ? kHalf : 32;
+    static_assert(NFW == 2 || NFW == 4, "fold warps per TMEM lane quadrant");
+    static_assert(kHalf >= 8 && kHalf % 8 == 0, "fold columns per warp");
     static_assert(kB % 1024 == 0, "stage alignment");
     static_assert((PST * kStage) % 1024 == 0 && kSStride % 128 == 0, "TMA destination alignment");
     static_assert(kSmem <= 232448, "shared memory budget");
@@ -137,12 +144,12 @@ __device__ __forceinline__ void tmem_ld_cols<8>(uint32_t taddr, uint32_t* r)
                  : "r"(taddr));
 }
 
-template <int BN, int PST>
-__global__ void __launch_bounds__(384, 1)
+template <int BN, int PST, int NFW>
+__global__ void __launch_bounds__(32 * (4 + 4 * NFW), 1)
     blk_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                     const __grid_constant__ CUtensorMap tm_s, const BlkParams p)
 {
-    using Tr = BlkTraits<BN, PST>;
+    using Tr = BlkTraits<BN, PST, NFW>;
     constexpr int NBUF = Tr::kNbuf;
     // token tiles of 128 are used only without a K split (the host picks
     // ksplit = 1 for them), so their reduction needs no register array
@@ -176,11 +183,11 @@ __global__ void __launch_bounds__(384, 1)
         }
         for (int i = 0; i < NS; ++i) {
             mbar_init(smem_u32(&sfull[i]), 1);
-            mbar_init(smem_u32(&sfree[i]), 8);
+            mbar_init(smem_u32(&sfree[i]), Tr::kFold);
         }
         for (int i = 0; i < NBUF; ++i) {
             mbar_init(smem_u32(&dfull[i]), 1);
-            mbar_init(smem_u32(&dempty[i]), 8);
+            mbar_init(smem_u32(&dempty[i]), Tr::kFold);
         }
         mbar_init(smem_u32(&drain[0]), 1);
         mbar_init(smem_u32(&drain[1]), 1);
@@ -332,8 +339,9 @@ __global__ void __launch_bounds__(384, 1)
         grid_dep_wait();   // the partials and counters are this call's workspace
         grid_dep_launch();
         const int q = warp & 3;
-        const int hh = (warp - 4) >> 2;
+        const int hh = (warp - 4) >> 2;          // column group of this warp
         const int c0 = hh * Tr::kHalf;
+        constexpr int kFoldThreads = 32 * Tr::kFold;
         int ss = 0;
         uint32_t sph = 0, kc = 0;
         bool ok = true;
@@ -415,7 +423,7 @@ __global__ void __launch_bounds__(384, 1)
             // threads' stores before one thread's fence + counter increment
             // (release); the CTA that completes the count fences (acquire)
             // before a second barrier releases its threads to read.
-            if (bar_any(1, 256, !ok)) {
+            if (bar_any(1, kFoldThreads, !ok)) {
                 ok = false;
                 break;
             }
@@ -427,9 +435,9 @@ __global__ void __launch_bounds__(384, 1)
                     __threadfence();
                 *s_last = last;
             }
-            asm volatile("bar.sync 1, 256;" ::: "memory");
+            asm volatile("bar.sync 1, %0;" ::"r"(kFoldThreads) : "memory");
             if (*s_last) {
-                // the tile's outputs are spread over the 256 fold threads (n
+                // the tile's outputs are spread over the fold threads (n
                 // fastest: coalesced); each requests all of an output's split
                 // partials before adding them in split order
                 const int mrows = min(BN, p.M - mt * BN);
@@ -437,7 +445,7 @@ __global__ void __launch_bounds__(384, 1)
                 // 4 consecutive outputs per item (16-byte loads), every split
                 // of an item requested before its sum, splits added in order
 #pragma unroll 2
-                for (int o = threadIdx.x - 128; o < 32 * mrows; o += 256) {
+                for (int o = threadIdx.x - 128; o < 32 * mrows; o += kFoldThreads) {
                     const int m = mt * BN + (o >> 5);
                     const int nn = nb * 128 + (o & 31) * 4;
                     const float4* src = reinterpret_cast<const float4*>(p.ypart + static_cast<int64_t>(m) * p.N + nn);
@@ -527,15 +535,15 @@ BlkConfig blk_pick_config(int M, int N, int K, int num_sms)
     return c;
 }
 
-template <int BN, int PST>
+template <int BN, int PST, int NFW>
 static int launch_blk(const CUtensorMap& tw, const CUtensorMap& tx, const CUtensorMap& ts,
                       const BlkParams& prm, int grid, cudaStream_t s)
 {
-    using Tr = BlkTraits<BN, PST>;
-    auto kern = blk_gemm_kernel<BN, PST>;
+    using Tr = BlkTraits<BN, PST, NFW>;
+    auto kern = blk_gemm_kernel<BN, PST, NFW>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Tr::kSmem) != cudaSuccess)
         return kErrLaunch;
-    return launch_dependent(kern, dim3(grid), dim3(384), Tr::kSmem, s, tw, tx, ts, prm) == cudaSuccess
+    return launch_dependent(kern, dim3(grid), dim3(Tr::kThreads), Tr::kSmem, s, tw, tx, ts, prm) == cudaSuccess
                ? kOK
                : kErrLaunch;
 }
@@ -571,10 +579,10 @@ int launch_block_gemm(const BlkLaunch& L, const BlkConfig& cfg, int num_sms, cud
     const int64_t tiles = static_cast<int64_t>(p.nb_count) * p.mt_count * p.ksplit;
     const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
     switch (BN) {
-    case 16: return launch_blk<16, 8>(tw, tx, ts, p, grid, s);
-    case 32: return launch_blk<32, 8>(tw, tx, ts, p, grid, s);
-    case 64: return launch_blk<64, 8>(tw, tx, ts, p, grid, s);
-    default: return launch_blk<128, 6>(tw, tx, ts, p, grid, s);
+    case 16: return launch_blk<16, 8, 2>(tw, tx, ts, p, grid, s);
+    case 32: return launch_blk<32, 8, 2>(tw, tx, ts, p, grid, s);
+    case 64: return launch_blk<64, 8, 2>(tw, tx, ts, p, grid, s);
+    default: return launch_blk<128, 6, 4>(tw, tx, ts, p, grid, s);
     }
 }
 

@@ -81,6 +81,10 @@ struct MoeGemmParams {
     int rows_per_expert2, rt_count2, kblocks2, ksplit2;
     int* done;               // [E] gate_up tiles finished per expert, x4 (one per epilogue warp)
     int* claim;              // [2] MODE 3: tiles claimed, CTAs done claiming (both zero between launches)
+    // tile-order bands inside an expert (0: none): gate_up walks all weight
+    // rows for `band` token tiles at a time, down all token tiles for `band`
+    // weight-row tiles at a time (band2: the down tiles of MODE 3)
+    int band, band2;
     uint32_t* err;
 };
 
@@ -158,14 +162,17 @@ struct TileInfo {
 
 // Tile t of the CTA-shared tile list -> (expert, 128-row weight tile, token
 // tile, K split). Tiles run in expert order. Inside an expert, gate_up walks
-// weight rows outermost (the expert's gathered activations are small and stay
-// in L2 while its weight tiles stream once); down walks token tiles outermost,
-// so the CTAs working at the same time share a few token tiles of the
-// intermediate activation (which, for a long prefill, is far larger than L2)
-// and stream the weight rows, whose deeper ring hides HBM latency.
+// weight rows outermost (the expert's gathered activations stay in L2 while its
+// weight tiles stream once); down walks token tiles outermost, so the CTAs
+// working at the same time share a few token tiles of the intermediate
+// activation and stream the weight rows, whose deeper ring hides HBM latency.
+// With a band (prefill, where one expert's activations exceed what L2 keeps):
+// gate_up takes `band` token tiles at a time and walks all weight rows over
+// them, down takes `band` weight-row tiles at a time and walks all token tiles
+// over them, so both operands of the tiles in flight are reused from L2.
 template <int MODE>
 __device__ __forceinline__ TileInfo decode_tile(int t, const int* s_cnt, const int* s_off,
-                                                const int* s_pre, int E, int BN, int ksplit, int rt_count)
+                                                const int* s_pre, int E, int BN, int ksplit, int rt_count, int band)
 {
     TileInfo ti;
     int e = 0;
@@ -176,17 +183,27 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const int* s_cnt, const i
     const int ntt = (c + BN - 1) / BN;
     ti.e = e;
     if (MODE != 1) {   // gate_up (static or dynamic scale)
-        const int per_rt = ntt * ksplit;
-        ti.rt = local / per_rt;
-        const int r2 = local - ti.rt * per_rt;
-        ti.tt = r2 / ksplit;
-        ti.ks = r2 - ti.tt * ksplit;
+        const int tb = band > 0 ? band : ntt;               // token tiles per band
+        const int per_band = rt_count * tb * ksplit;        // tiles of a full band
+        const int bi = local / per_band;
+        const int rem = local - bi * per_band;
+        const int w = min(tb, ntt - bi * tb);               // token tiles of this band
+        const int per_rt = w * ksplit;
+        ti.rt = rem / per_rt;
+        const int r2 = rem - ti.rt * per_rt;
+        ti.tt = bi * tb + r2 / ksplit;
+        ti.ks = r2 - (r2 / ksplit) * ksplit;
     } else {
-        const int per_tt = rt_count * ksplit;
-        ti.tt = local / per_tt;
-        const int r2 = local - ti.tt * per_tt;
-        ti.rt = r2 / ksplit;
-        ti.ks = r2 - ti.rt * ksplit;
+        const int rb = band > 0 ? band : rt_count;          // weight-row tiles per band
+        const int per_band = rb * ntt * ksplit;
+        const int bi = local / per_band;
+        const int rem = local - bi * per_band;
+        const int w = min(rb, rt_count - bi * rb);          // row tiles of this band
+        const int per_tt = w * ksplit;
+        ti.tt = rem / per_tt;
+        const int r2 = rem - ti.tt * per_tt;
+        ti.rt = bi * rb + r2 / ksplit;
+        ti.ks = r2 - (r2 / ksplit) * ksplit;
     }
     ti.tok0 = s_off[e] + ti.tt * BN;
     ti.ntok = min(BN, c - ti.tt * BN);
@@ -212,13 +229,13 @@ __device__ __forceinline__ TileInfo decode_any(int t, bool gu, const int* s_cnt,
                                                const int* s_pre2, int n_gu, int BN, const MoeGemmParams& p)
 {
     if constexpr (MODE == 3) {
-        return gu ? decode_tile<0>(t, s_cnt, s_off, s_pre, p.E, BN, 1, p.rt_count)
-                  : decode_tile<1>(t - n_gu, s_cnt, s_off, s_pre2, p.E, BN, p.ksplit2, p.rt_count2);
+        return gu ? decode_tile<0>(t, s_cnt, s_off, s_pre, p.E, BN, 1, p.rt_count, p.band)
+                  : decode_tile<1>(t - n_gu, s_cnt, s_off, s_pre2, p.E, BN, p.ksplit2, p.rt_count2, p.band2);
     } else {
         (void)gu;
         (void)s_pre2;
         (void)n_gu;
-        return decode_tile<MODE>(t, s_cnt, s_off, s_pre, p.E, BN, p.ksplit, p.rt_count);
+        return decode_tile<MODE>(t, s_cnt, s_off, s_pre, p.E, BN, p.ksplit, p.rt_count, p.band);
     }
 }
 
@@ -306,6 +323,9 @@ __global__ void __launch_bounds__(32 * (4 + NCONV + NEPI), 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // prefill tiles (A by TMA) wait with a suspend hint: their epilogue warps
+    // wait through whole tiles and would otherwise take issue slots
+    constexpr uint32_t kHint = Tr::kA8 ? 20000u : 0u;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NW; ++i) {
@@ -438,7 +458,7 @@ __global__ void __launch_bounds__(32 * (4 + NCONV + NEPI), 1)
                 for (int kb = wi.kb0; kb < wi.kb0 + wi.nkb; ++kb) {
                     if (wi.claim_here(kb, 4))
                         wi.claim_next();
-                    if (!mbar_wait_or_abort(smem_u32(&freeb[s]), ph ^ 1u, s_abort)) {
+                    if (!mbar_wait_or_abort<kHint>(smem_u32(&freeb[s]), ph ^ 1u, s_abort)) {
                         ok = false;
                         break;
                     }
@@ -529,7 +549,7 @@ __global__ void __launch_bounds__(32 * (4 + NCONV + NEPI), 1)
                 const uint32_t idesc = idesc_e4m3_f32(128, nmma);
                 const int d = it & 1;
                 const uint32_t use = static_cast<uint32_t>(it >> 1);
-                if (!mbar_wait_or_abort(smem_u32(&accempty[d]), (use & 1u) ^ 1u, s_abort)) {
+                if (!mbar_wait_or_abort<kHint>(smem_u32(&accempty[d]), (use & 1u) ^ 1u, s_abort)) {
                     ok = false;
                     break;
                 }
@@ -538,8 +558,8 @@ __global__ void __launch_bounds__(32 * (4 + NCONV + NEPI), 1)
                 bool first = true;
                 for (int kb = 0; kb < wi.nkb; ++kb, ++g) {
                     if (static_cast<int>(g % NISS) == me) {
-                        if (!mbar_wait_or_abort(smem_u32(&afull[x]), ph, s_abort) ||
-                            ((Tr::kSplitB || Tr::kA8) && !mbar_wait_or_abort(smem_u32(&bfull[b]), bph, s_abort))) {
+                        if (!mbar_wait_or_abort<kHint>(smem_u32(&afull[x]), ph, s_abort) ||
+                            ((Tr::kSplitB || Tr::kA8) && !mbar_wait_or_abort<kHint>(smem_u32(&bfull[b]), bph, s_abort))) {
                             ok = false;
                             break;
                         }
@@ -610,8 +630,8 @@ __global__ void __launch_bounds__(32 * (4 + NCONV + NEPI), 1)
                     // the A slot is free once the MMAs of its previous round
                     // completed: seen through that round's activation copy
                     // (shared ring), or the MMA's commit (separate ring)
-                    if (!mbar_wait_or_abort(smem_u32(&wfull[w]), wph, s_abort) ||
-                        !mbar_wait_or_abort(smem_u32(Tr::kSplitB ? &xfree[x] : &bfull[x]),
+                    if (!mbar_wait_or_abort<kHint>(smem_u32(&wfull[w]), wph, s_abort) ||
+                        !mbar_wait_or_abort<kHint>(smem_u32(Tr::kSplitB ? &xfree[x] : &bfull[x]),
                                             Tr::kSplitB ? (xph ^ 1u) : xph, s_abort)) {
                         ok = false;
                         break;
@@ -692,7 +712,7 @@ __global__ void __launch_bounds__(32 * (4 + NCONV + NEPI), 1)
             const TileInfo ti = decode_any<MODE>(wi.t, gu, s_cnt, s_off, s_pre, s_pre2, n_gu, BN, p);
             const int d = it & 1;
             const uint32_t use = static_cast<uint32_t>(it >> 1);
-            if (!mbar_wait_or_abort(smem_u32(&accfull[d]), use & 1u, s_abort)) {
+            if (!mbar_wait_or_abort<kHint>(smem_u32(&accfull[d]), use & 1u, s_abort)) {
                 ok = false;
                 break;
             }
@@ -1171,6 +1191,11 @@ static int fused_ksplit(int T, int H, int I, int E, int k, int bn, int kc, int n
 
 bool moe_unpack_once(int T) { return T > 128; }
 
+// Prefill tile-order band (see decode_tile): 16 token tiles of 256 tokens
+// (about 25 MB of gathered activations at hidden 6144) for gate_up, 16
+// weight-row tiles for down.
+constexpr int kPrefillBand = 16;
+
 MoeConfig moe_pick_config(int T, int H, int I, int E, int k, int num_sms, bool one_launch)
 {
     MoeConfig c;
@@ -1365,6 +1390,7 @@ int launch_moe_forward(const MoeLaunch& L, const MoeConfig& cfg, int num_sms, cu
     gu.rt_count = L.I / 64;
     gu.kblocks = (L.H + KC - 1) / KC;
     gu.ksplit = 1;
+    gu.band = a8 ? kPrefillBand : 0;
     int64_t tiles = static_cast<int64_t>(gu.rt_count) * tok_tiles_max;
     int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
     int st = L.dynamic ? dispatch_gemm<2>(cfg, tw_gu, tb_gu, tw_gu, tb_gu, gu, grid, s)
@@ -1385,6 +1411,7 @@ int launch_moe_forward(const MoeLaunch& L, const MoeConfig& cfg, int num_sms, cu
     dn.kblocks = (L.I + KC - 1) / KC / dn.ksplit;
     dn.streamk = cfg.streamk;
     dn.nslots = cfg.nslots;
+    dn.band = a8 ? kPrefillBand : 0;
     tiles = static_cast<int64_t>(dn.rt_count) * tok_tiles_max * dn.ksplit;
     grid = cfg.streamk ? num_sms : static_cast<int>(tiles < num_sms ? tiles : num_sms);
     st = dispatch_gemm<1>(cfg, tw_d, tb_d, tw_d, tb_d, dn, grid, s);
