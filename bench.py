@@ -210,11 +210,13 @@ class ClockSampler:
         rows = [r[1] for r in rows]
         sm = [num(r[0]) for r in rows if num(r[0]) is not None]
         mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        pw = [num(r[2]) for r in rows if len(r) > 2 and num(r[2]) is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4)
                           if len(r) > 3 + i and r[3 + i].lower().startswith("active")})
         return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows),
+                "power_w": statistics.median(pw) if pw else None}
 
 
 def load_peaks():

@@ -1034,7 +1034,6 @@ __global__ void __launch_bounds__(256) moe_hquant_kernel(const float* __restrict
 // launches back), so they are fetched before the dependency wait; only the
 // partial sums and s0h, which the GEMM writes, are read after it.
 // ---------------------------------------------------------------------------
-constexpr int kFinPre = 8;   // assignments per token fetched before the wait (k <= 8)
 
 template <int KS_MAX>
 __device__ __forceinline__ void fin_accumulate(float (&acc)[4], int pos, float wt, float4 sd, float a2, int A, int H,
@@ -1068,7 +1067,10 @@ __device__ __forceinline__ void fin_accumulate(float (&acc)[4], int pos, float w
     }
 }
 
-template <int KS_MAX>
+// KPRE: assignments per token fetched before the dependency wait (the rest,
+// for k > KPRE, after it); sized by k so that the registers of unused slots
+// do not cost occupancy (a memory-bound pass needs its loads in flight).
+template <int KS_MAX, int KPRE>
 __global__ void __launch_bounds__(256) moe_finalize_kernel(
     int T, int H, int k, int A, int ksplit, const int32_t* __restrict__ ids,
     const float* __restrict__ topk_w, const int32_t* __restrict__ inv,
@@ -1080,14 +1082,14 @@ __global__ void __launch_bounds__(256) moe_finalize_kernel(
     const bool live = idx < static_cast<int64_t>(T) * per_row;
     const int t = live ? static_cast<int>(idx / per_row) : 0;
     const int n = live ? static_cast<int>(idx % per_row) * 4 : 0;
-    int pos_p[kFinPre];
-    float wt_p[kFinPre];
-    float4 sd_p[kFinPre];
+    int pos_p[KPRE];
+    float wt_p[KPRE];
+    float4 sd_p[KPRE];
     float a2 = 0.0f;
     if (live) {
         a2 = __ldg(a2p);
 #pragma unroll
-        for (int j = 0; j < kFinPre; ++j) {
+        for (int j = 0; j < KPRE; ++j) {
             if (j < k) {
                 const int a = t * k + j;
                 pos_p[j] = __ldg(inv + a);
@@ -1103,10 +1105,10 @@ __global__ void __launch_bounds__(256) moe_finalize_kernel(
         return;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int j = 0; j < kFinPre; ++j)
+    for (int j = 0; j < KPRE; ++j)
         if (j < k)
             fin_accumulate<KS_MAX>(acc, pos_p[j], wt_p[j], sd_p[j], a2, A, H, n, ksplit, ypart, s0h);
-    for (int j = kFinPre; j < k; ++j) {
+    for (int j = KPRE; j < k; ++j) {
         const int a = t * k + j;
         const int e = __ldg(ids + a);
         fin_accumulate<KS_MAX>(acc, __ldg(inv + a), __ldg(topk_w + a),
@@ -1423,9 +1425,12 @@ int launch_moe_forward(const MoeLaunch& L, const MoeConfig& cfg, int num_sms, cu
     const int64_t nthreads = static_cast<int64_t>(L.T) * (L.H / 4);
     // the register array of split partials is sized for the split in use
     const int parts = (cfg.streamk && !fused) ? cfg.nslots : cfg.ksplit;
-    auto fin = parts == 1 ? moe_finalize_kernel<1>
-             : parts <= 4 ? moe_finalize_kernel<4>
-             : parts <= 8 ? moe_finalize_kernel<8> : moe_finalize_kernel<kMaxKsplit>;
+    auto fin = L.k <= 2 ? (parts == 1 ? moe_finalize_kernel<1, 2>
+                           : parts <= 4 ? moe_finalize_kernel<4, 2>
+                           : parts <= 8 ? moe_finalize_kernel<8, 2> : moe_finalize_kernel<kMaxKsplit, 2>)
+                        : (parts == 1 ? moe_finalize_kernel<1, 8>
+                           : parts <= 4 ? moe_finalize_kernel<4, 8>
+                           : parts <= 8 ? moe_finalize_kernel<8, 8> : moe_finalize_kernel<kMaxKsplit, 8>);
     if (launch_dependent(fin, dim3(static_cast<unsigned>((nthreads + 255) / 256)), dim3(256), 0, s,
                          L.T, L.H, L.k, A, parts, L.ids, L.topk_w, L.inv, L.ypart,
                          static_cast<const unsigned long long*>(L.s0h), L.s_d,
