@@ -190,3 +190,21 @@ def test_grok_prefill_full_size_sampled(grok_weights):
     assert torch.isfinite(out.float()).all()
     check_hidden_codes(case, ws, toks, "grok prefill (512-token sample)")
     assert_close(bf16_to_f64(out[toks]), case.oracle_out(toks), "grok prefill (512-token sample)")
+
+
+def test_prefill_bands_with_partial_last_bands():
+    """The prefill plan's banded tile order across several bands: 9000 tokens
+    over 2 experts (k = 1) give each expert 18 token tiles of 256 (gate_up
+    bands of 16 + 2 token tiles) and H = 2560 gives 20 down row tiles (bands of
+    16 + 4); every token and every intermediate code is compared."""
+    import w4a8_moe_gb300 as lib
+    T, H, I, E, k = 9000, 2560, 512, 2, 1
+    assert lib.moe_w4a8_plan(T, H, I, E, k)["token_tile"] == 256
+    case = MoECase(T, H, I, E, k, 1, seed=77)
+    assert min(case.o_counts) > 16 * 256                       # more than one token band per expert
+    case.check_integer_parts()
+    ws = _workspace(case)
+    out = case.run_gpu(ws=ws)
+    toks = list(range(T))
+    check_hidden_codes(case, ws, toks, "prefill bands T9000 H2560")
+    assert_close(bf16_to_f64(out), case.oracle_out(toks), "prefill bands T9000 H2560")
