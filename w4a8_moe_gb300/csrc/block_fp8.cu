@@ -21,7 +21,10 @@
 // quadrant, each BN/NFW of the token columns: with more warps in flight the
 // latency of each K-block's TMEM load, scale load and barrier round trip is
 // hidden by the other warps' work). Swapped operands: M = 128 weight rows,
-// N = BN tokens.
+// N = BN tokens. With 128-token tiles one thread issues every MMA (an N = 128
+// MMA outlasts its issue) and warp 3 instead turns each landed scale slot, in
+// place, into the combined scales xs[m, g] * Wsi[nb, g], so the fold warps
+// need not each form them.
 //
 // When K is split over several CTAs, each writes its fp32 partial and bumps a
 // per-tile counter; the CTA that completes the count sums the partials in
@@ -54,7 +57,10 @@ struct BlkTraits {
     static constexpr int kSBytes = BN * 4;                               // one scale slot's copy
     static constexpr int kSStride = ((kSBytes + 127) / 128) * 128;       // TMA destinations: 128-byte aligned
     static constexpr int kData = PST * kStage + ((kNs * kSStride + 1023) / 1024) * 1024;
-    static constexpr int kBars = 3 * PST + 2 * kNs + 2 * kNbuf + 2;
+    static constexpr int kBars = 3 * PST + 3 * kNs + 2 * kNbuf + 2;
+    // warp 3: a second MMA issuer, or (128-token tiles) the combined-scale warp
+    static constexpr bool kScaleWarp = (BN >= 128);
+    static constexpr int kIssuers = kScaleWarp ? 1 : 2;
     // the two MMA-issuing threads take alternate K-blocks: every ring slot and
     // partial buffer must always belong to the same thread (parity waits)
     static_assert(PST % 2 == 0 && kNbuf % 2 == 0, "even ring depths for two issuers");
@@ -165,7 +171,8 @@ __global__ void __launch_bounds__(32 * (4 + 4 * NFW), 1)
     uint64_t* sempty = xfull + PST;     // weight + activation slot free (MMA commit)
     uint64_t* sfull = sempty + PST;     // scales landed  [NS]
     uint64_t* sfree = sfull + NS;       // scales consumed by the fold  [NS]
-    uint64_t* dfull = sfree + NS;       // partial product ready  [NBUF]
+    uint64_t* sready = sfree + NS;      // combined scales written (scale warp)  [NS]
+    uint64_t* dfull = sready + NS;      // partial product ready  [NBUF]
     uint64_t* dempty = dfull + NBUF;    // partial buffer folded  [NBUF]
     uint64_t* drain = dempty + NBUF;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain + 2);   // one drain barrier per issuer
@@ -184,6 +191,7 @@ __global__ void __launch_bounds__(32 * (4 + 4 * NFW), 1)
         for (int i = 0; i < NS; ++i) {
             mbar_init(smem_u32(&sfull[i]), 1);
             mbar_init(smem_u32(&sfree[i]), Tr::kFold);
+            mbar_init(smem_u32(&sready[i]), 1);
         }
         for (int i = 0; i < NBUF; ++i) {
             mbar_init(smem_u32(&dfull[i]), 1);
@@ -288,11 +296,12 @@ __global__ void __launch_bounds__(32 * (4 + 4 * NFW), 1)
                         mbar_wait(smem_u32(&sfull[s]), (s_last_par >> s) & 1u);
             }
         }
-    } else if (warp == 1 || warp == 3) {
+    } else if (warp == 1 || (!Tr::kScaleWarp && warp == 3)) {
         // ------------------------------------------------------------ MMA issuers
         // Every K-block has its own partial buffer, so two threads can issue:
         // warp 1 takes the even K-blocks of the CTA's sequence, warp 3 the odd
-        // ones, which hides each thread's barrier waits behind the other's MMAs.
+        // ones, which hides each thread's barrier waits behind the other's MMAs
+        // (short N = 16..64 MMAs); for 128-token tiles warp 1 issues them all.
         if (lane == 0) {
             const int me = (warp == 1) ? 0 : 1;
             const uint32_t idesc = idesc_e4m3_f32(128, BN);
@@ -301,7 +310,7 @@ __global__ void __launch_bounds__(32 * (4 + 4 * NFW), 1)
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 for (int kb = 0; kb < p.kb_per_split; ++kb, ++kc) {
-                    if (static_cast<int>(kc & 1u) != me) {
+                    if (static_cast<int>(kc % Tr::kIssuers) != me) {
                         if (++ps == PST) {
                             ps = 0;
                             ph ^= 1u;
@@ -338,6 +347,44 @@ __global__ void __launch_bounds__(32 * (4 + 4 * NFW), 1)
                 mbar_wait(smem_u32(&drain[me]), 0);
             }
         }
+    } else if (Tr::kScaleWarp && warp == 3) {
+        // ------------------------------------------------------------ combined scales
+        // sc[m] = xs[m, g] * Wsi[nb, g] (fp32, round to nearest: the product the
+        // fold would form), written over the landed activation scales; the
+        // slot is refilled by TMA only after every fold warp released it.
+        int ss = 0;
+        uint32_t sph = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const int nb = t / per_nb, ks = (t % per_nb) % p.ksplit;
+            for (int kb = 0; kb < p.kb_per_split; ++kb) {
+                if (!mbar_wait_or_abort<2000u>(smem_u32(&sfull[ss]), sph, s_abort)) {
+                    ok = false;
+                    break;
+                }
+                const int g = ks * p.kb_per_split + kb;
+                const float ws = __ldg(p.wsi + static_cast<int64_t>(nb) * p.KB + g);
+                float4* xs4 = reinterpret_cast<float4*>(sring + ss * Tr::kSStride);
+                if (4 * lane < BN) {
+                    float4 v = xs4[lane];
+                    v.x *= ws;
+                    v.y *= ws;
+                    v.z *= ws;
+                    v.w *= ws;
+                    xs4[lane] = v;
+                }
+                fence_proxy_async_smem();   // ordered before the slot's next TMA fill
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_u32(&sready[ss]));
+                if (++ss == NS) {
+                    ss = 0;
+                    sph ^= 1u;
+                }
+            }
+        }
+        if (!ok)
+            fail();
     } else if (warp >= 4) {
         // ------------------------------------------------------------ fold + store
         grid_dep_wait();   // the partials and counters are this call's workspace
@@ -352,7 +399,7 @@ __global__ void __launch_bounds__(32 * (4 + 4 * NFW), 1)
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
             const int nb = t / per_nb, r = t % per_nb, mt = r / p.ksplit, ks = r % p.ksplit;
             // column pairs, folded with packed fp32x2 arithmetic (each lane of a
-            // pair rounds exactly like the scalar fmaf(p, xs * ws, acc))
+            // pair rounds exactly like the scalar fmaf(p, sc, acc), sc = xs * ws)
             uint64_t acc2[Tr::kHalf / 2];
 #pragma unroll
             for (int c = 0; c < Tr::kHalf / 2; ++c)
@@ -361,7 +408,7 @@ __global__ void __launch_bounds__(32 * (4 + 4 * NFW), 1)
                 const int d = static_cast<int>(kc % NBUF);
                 const uint32_t use = kc / NBUF;
                 if (!mbar_wait_or_abort(smem_u32(&dfull[d]), use & 1u, s_abort) ||
-                    !mbar_wait_or_abort(smem_u32(&sfull[ss]), sph, s_abort)) {
+                    !mbar_wait_or_abort(smem_u32(Tr::kScaleWarp ? &sready[ss] : &sfull[ss]), sph, s_abort)) {
                     ok = false;
                     break;
                 }
@@ -380,7 +427,7 @@ __global__ void __launch_bounds__(32 * (4 + 4 * NFW), 1)
                     const uint64_t* xs2 = reinterpret_cast<const uint64_t*>(xs + c0 + ch * Tr::kChunk);
 #pragma unroll
                     for (int c = 0; c < Tr::kChunk / 2; ++c) {
-                        const uint64_t sc = f2_mul(xs2[c], ws2);
+                        const uint64_t sc = Tr::kScaleWarp ? xs2[c] : f2_mul(xs2[c], ws2);
                         const uint64_t pv = f2_pack(__uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1]));
                         acc2[ch * Tr::kChunk / 2 + c] = f2_fma(pv, sc, acc2[ch * Tr::kChunk / 2 + c]);
                     }
