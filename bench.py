@@ -119,9 +119,9 @@ def throughput(world: int, tokens_per_rank: int, steps: int, ms_slowest: float) 
 NCU_TRAFFIC = {
     "sources": ["w4a8_moe_gb300/csrc/moe.cu", "w4a8_moe_gb300/csrc/ptx.cuh", "w4a8_moe_gb300/csrc/sched.cuh",
                 "w4a8_moe_gb300/csrc/internal.h"],
-    "sha256": "00f06af38cfba3e05045d6005a719b7d8e724de2c2a01f130e4340fb02903aad",
-    "grok_prefill:gate_up": 17653629952 + 2106472960,
-    "mixtral_decode:one_launch": 705905408 + 4983296,
+    "sha256": "e19025028ed6dd85715727453857e3c28f06c61d8ae4f15ecc60863a9535ff63",
+    "grok_prefill:gate_up": 18544088064 + 2107783680,
+    "mixtral_decode:one_launch": 705905408 + 4946432,
 }
 
 

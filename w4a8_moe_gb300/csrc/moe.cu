@@ -105,7 +105,9 @@ struct MoeTraits {
     static constexpr bool kSplitB = (NB != NX);
     // No converter warps (NCONV = 0): A arrives by TMA from weights unpacked
     // ahead of the GEMM (moe_upcast_kernel) into the shared-memory A slots,
-    // loaded by warp 0 in place of the packed weight stream (no W ring).
+    // loaded by warp 0 in place of the packed weight stream (no W ring). Those
+    // hold the signed INT4 values as E4M3 codes, so the accumulators need no
+    // shift and the intermediate no exact row sums.
     static constexpr bool kA8 = (NCONV == 0);
     static constexpr int kData = NW * kWBytes + NB * kXBytes + (NX - NXT) * kASlot;
     static constexpr int kBars = 2 * NW + 2 * NB + 2 * NX + 4 + 2 + 2 * kTileQ;   // + drain, tile queue
@@ -751,9 +753,11 @@ __global__ void __launch_bounds__(32 * (4 + NCONV + NEPI), 1)
                 for (int ch = sub; ch < nchunks; ch += kChStep) {
                     // lane l fetches the exact shift of column ch*32 + l up front
                     // (the loop below hands it around by shuffle), so no load
-                    // waits behind the byte stores of the loop
+                    // waits behind the byte stores of the loop; weights unpacked
+                    // ahead (A by TMA) carry their signed values, no shift
                     const int mycol = ch * 32 + lane;
-                    const long long my_s0x = (mycol < ti.ntok) ? __ldg(p.s0x + ti.tok0 + mycol) : 0LL;
+                    const long long my_s0x =
+                        (!Tr::kA8 && mycol < ti.ntok) ? __ldg(p.s0x + ti.tok0 + mycol) : 0LL;
                     uint32_t v[32];
                     load_acc(ch * 32, v);
                     const float my_shift = static_cast<float>(my_s0x) * (1.0f / 64.0f);
@@ -767,12 +771,12 @@ __global__ void __launch_bounds__(32 * (4 + NCONV + NEPI), 1)
                         const float pg = half ? recv : __uint_as_float(v[cc]);
                         const float pu = half ? __uint_as_float(v[cc + 16]) : recv;
                         const int col = ch * 32 + cc + 16 * half;
-                        const float shift = __shfl_sync(0xFFFFFFFFu, my_shift, cc + 16 * half);
+                        const float shift = Tr::kA8 ? 0.0f : __shfl_sync(0xFFFFFFFFu, my_shift, cc + 16 * half);
                         s512[cc] = 0.0f;
                         if (col < ti.ntok) {
                             const int pos = ti.tok0 + col;
-                            const float G = fmaf(512.0f, pg, -shift);
-                            const float U = fmaf(512.0f, pu, -shift);
+                            const float G = Tr::kA8 ? pg : fmaf(512.0f, pg, -shift);
+                            const float U = Tr::kA8 ? pu : fmaf(512.0f, pu, -shift);
                             const float h = act_fn(sg * G, p.act) * (su * U);
                             if constexpr (MODE == 2) {
                                 p.hf[static_cast<int64_t>(pos) * p.I + i] = h;
@@ -781,7 +785,8 @@ __global__ void __launch_bounds__(32 * (4 + NCONV + NEPI), 1)
                                 // hq = E4M3(h / a2): IEEE division, then one RNE rounding
                                 const uint32_t code = cvt_e4m3(__fdiv_rn(h, a2));
                                 p.hq[static_cast<int64_t>(pos) * p.I + kperm(i)] = static_cast<uint8_t>(code);
-                                s512[cc] = e4m3_times512_f32(code);
+                                if constexpr (!Tr::kA8)
+                                    s512[cc] = e4m3_times512_f32(code);
                             }
                         }
                     }
@@ -791,7 +796,7 @@ __global__ void __launch_bounds__(32 * (4 + NCONV + NEPI), 1)
                             hmax_l = fmaxf(hmax_l, __shfl_xor_sync(0xFFFFFFFFu, hmax_l, o));
                         if (lane == 0 && hmax_l > 0.0f)   // non-negative floats order like their bits
                             atomicMax(p.hmax, __float_as_uint(hmax_l));
-                    } else {
+                    } else if constexpr (!Tr::kA8) {   // the down GEMM's shift: exact row sums of hq
                         // reduce-scatter over the 16 lanes of each half: lane ends
                         // with the sum of column ch*32 + lane over this warp's rows
 #pragma unroll
@@ -925,14 +930,29 @@ __global__ void __launch_bounds__(128) moe_gather_kernel(const uint8_t* __restri
 
 // ---------------------------------------------------------------------------
 // Prefill: the INT4 weights of every expert with tokens, unpacked once per call
-// into the E4M3 operand bytes the GEMM's converters produce (value
-// (q + 8) * 2^-9, codes of a packed word in the order of unpack8), so that the
-// GEMM loads A by TMA and its tiles each reuse it instead of unpacking it again
-// for every token tile. gate_up rows are stored in tile order: 128-row tile rt
-// holds, for each TMEM lane quadrant q, gate rows rt*64 + 16q + 0..15 and then
-// the matching up rows (the pairing of the gated epilogue). One thread per 16
-// packed bytes (32 weights) of a row.
+// into E4M3 codes of their signed values q (every INT4 value is exact in E4M3),
+// codes of a packed word in the K order of unpack8, so that the GEMM loads A by
+// TMA and its tiles each reuse it instead of unpacking it again for every token
+// tile; with signed values the products need no offset correction. gate_up rows
+// are stored in tile order: 128-row tile rt holds, for each TMEM lane quadrant
+// q, gate rows rt*64 + 16q + 0..15 and then the matching up rows (the pairing of
+// the gated epilogue). One thread per 16 packed bytes (32 weights) of a row.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t e4m3_of_int4_pair4(uint32_t w, int first)
+{
+    // nibbles first, first + 2, first + 4, first + 6 of w -> their E4M3 codes
+    float f[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        f[j] = static_cast<float>(static_cast<int32_t>(w << (28 - 4 * (first + 2 * j))) >> 28);
+    return static_cast<uint32_t>(cvt_e4m3x2(f[1], f[0])) | (static_cast<uint32_t>(cvt_e4m3x2(f[3], f[2])) << 16);
+}
+__device__ __forceinline__ void unpack8_signed(uint32_t w, uint32_t& lo4, uint32_t& hi4)
+{
+    lo4 = e4m3_of_int4_pair4(w, 0);   // codes 0,2,4,6
+    hi4 = e4m3_of_int4_pair4(w, 1);   // codes 1,3,5,7
+}
+
 __global__ void __launch_bounds__(256) moe_upcast_kernel(const int32_t* __restrict__ w_gu,
                                                          const int32_t* __restrict__ w_d, int E, int H, int I,
                                                          const int32_t* __restrict__ counts,
@@ -964,10 +984,10 @@ __global__ void __launch_bounds__(256) moe_upcast_kernel(const int32_t* __restri
         const int32_t* w = gu ? w_gu : w_d;
         const uint4 v = __ldg(reinterpret_cast<const uint4*>(w + (static_cast<int64_t>(e) * rows + src) * (K / 8)) + j);
         uint32_t o[8];
-        unpack8(v.x, o[0], o[1]);
-        unpack8(v.y, o[2], o[3]);
-        unpack8(v.z, o[4], o[5]);
-        unpack8(v.w, o[6], o[7]);
+        unpack8_signed(v.x, o[0], o[1]);
+        unpack8_signed(v.y, o[2], o[3]);
+        unpack8_signed(v.z, o[4], o[5]);
+        unpack8_signed(v.w, o[6], o[7]);
         uint4* dst = reinterpret_cast<uint4*>((gu ? a_gu : a_d) + row * K) + 2 * j;
         dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
         dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
@@ -1028,7 +1048,9 @@ __global__ void __launch_bounds__(256) moe_hquant_kernel(const float* __restrict
 
 // ---------------------------------------------------------------------------
 // Combine: out[t, n] = bf16( sum_j w[t,j] * a2 * S_d[e,n] * D ),
-// D = 512 * sum_splits P - s0h/64, in j then split order (deterministic).
+// D = 512 * sum_splits P - s0h/64 (weights with the +8 offset, unpacked in the
+// GEMM), or D = sum_splits P (signed weights unpacked ahead: s0h = null,
+// pmul = 1), in j then split order (deterministic).
 // The routing arrays come from a kernel at least two launches back and S_d
 // and a2 from no kernel of this forward (or, for the dynamic scale, two
 // launches back), so they are fetched before the dependency wait; only the
@@ -1038,7 +1060,7 @@ __global__ void __launch_bounds__(256) moe_hquant_kernel(const float* __restrict
 template <int KS_MAX>
 __device__ __forceinline__ void fin_accumulate(float (&acc)[4], int pos, float wt, float4 sd, float a2, int A, int H,
                                                int n, int ksplit, const float* __restrict__ ypart,
-                                               const unsigned long long* __restrict__ s0h)
+                                               const unsigned long long* __restrict__ s0h, float pmul)
 {
     // all split partials (at most KS_MAX) are requested before the first one
     // is added, then summed in split order
@@ -1047,7 +1069,7 @@ __device__ __forceinline__ void fin_accumulate(float (&acc)[4], int pos, float w
     for (int s = 0; s < KS_MAX; ++s)
         if (s < ksplit)
             v[s] = __ldg(reinterpret_cast<const float4*>(ypart + (static_cast<int64_t>(s) * A + pos) * H + n));
-    const float shift = static_cast<float>(static_cast<long long>(__ldg(s0h + pos))) * (1.0f / 64.0f);
+    const float shift = s0h ? static_cast<float>(static_cast<long long>(__ldg(s0h + pos))) * (1.0f / 64.0f) : 0.0f;
     float4 P = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int s = 0; s < KS_MAX; ++s) {
@@ -1062,7 +1084,7 @@ __device__ __forceinline__ void fin_accumulate(float (&acc)[4], int pos, float w
     const float Sv[4] = {sd.x, sd.y, sd.z, sd.w};
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-        const float D = fmaf(512.0f, Pv[c], -shift);
+        const float D = fmaf(pmul, Pv[c], -shift);
         acc[c] = fmaf(wt, a2 * Sv[c] * D, acc[c]);
     }
 }
@@ -1074,7 +1096,7 @@ template <int KS_MAX, int KPRE>
 __global__ void __launch_bounds__(256) moe_finalize_kernel(
     int T, int H, int k, int A, int ksplit, const int32_t* __restrict__ ids,
     const float* __restrict__ topk_w, const int32_t* __restrict__ inv,
-    const float* __restrict__ ypart, const unsigned long long* __restrict__ s0h,
+    const float* __restrict__ ypart, const unsigned long long* __restrict__ s0h, float pmul,
     const float* __restrict__ s_d, const float* __restrict__ a2p, uint16_t* __restrict__ out)
 {
     const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -1107,13 +1129,13 @@ __global__ void __launch_bounds__(256) moe_finalize_kernel(
 #pragma unroll
     for (int j = 0; j < KPRE; ++j)
         if (j < k)
-            fin_accumulate<KS_MAX>(acc, pos_p[j], wt_p[j], sd_p[j], a2, A, H, n, ksplit, ypart, s0h);
+            fin_accumulate<KS_MAX>(acc, pos_p[j], wt_p[j], sd_p[j], a2, A, H, n, ksplit, ypart, s0h, pmul);
     for (int j = KPRE; j < k; ++j) {
         const int a = t * k + j;
         const int e = __ldg(ids + a);
         fin_accumulate<KS_MAX>(acc, __ldg(inv + a), __ldg(topk_w + a),
                                __ldg(reinterpret_cast<const float4*>(s_d + static_cast<int64_t>(e) * H + n)), a2, A,
-                               H, n, ksplit, ypart, s0h);
+                               H, n, ksplit, ypart, s0h, pmul);
     }
     uint2 o;
     o.x = static_cast<uint32_t>(float_to_bf16_bits(acc[0])) |
@@ -1433,7 +1455,8 @@ int launch_moe_forward(const MoeLaunch& L, const MoeConfig& cfg, int num_sms, cu
                            : parts <= 8 ? moe_finalize_kernel<8, 8> : moe_finalize_kernel<kMaxKsplit, 8>);
     if (launch_dependent(fin, dim3(static_cast<unsigned>((nthreads + 255) / 256)), dim3(256), 0, s,
                          L.T, L.H, L.k, A, parts, L.ids, L.topk_w, L.inv, L.ypart,
-                         static_cast<const unsigned long long*>(L.s0h), L.s_d,
+                         // weights unpacked ahead carry signed values: no shift
+                         a8 ? nullptr : static_cast<const unsigned long long*>(L.s0h), a8 ? 1.0f : 512.0f, L.s_d,
                          L.dynamic ? static_cast<const float*>(L.a2_out) : L.a2, L.out) != cudaSuccess)
         return kErrLaunch;
     mark(3);
