@@ -49,12 +49,17 @@ def run(M, N, K, rows=None, seed=0):
 @pytest.mark.parametrize("N,K", synth.BLOCK_FP8_SHAPES)
 @pytest.mark.parametrize("M", synth.BLOCK_FP8_M)
 def test_block_fp8_configs(M, N, K):
-    rows = None if M <= 8 else [0, 1, M // 2, M - 1]
+    # sampled rows: every 32-row quadrant of a 128-token tile (its TMEM lane
+    # group) appears, in the first, a middle and the last tile
+    rows = None if M <= 8 else sorted({r for r in (0, 1, 37, 70, 101, 127, M // 2 + 45, M - 90, M - 1)
+                                       if 0 <= r < M})
     run(M, N, K, rows=rows)
 
 
 @pytest.mark.parametrize("M,N,K", [(3, 128, 128), (17, 256, 384), (100, 384, 1024),
-                                   (130, 128, 256), (65, 512, 2560)])
+                                   (130, 128, 256), (65, 512, 2560),
+                                   (300, 768, 384),     # 256-row weight tiles, 3 token tiles, ragged last
+                                   (257, 640, 1024)])   # 128-row weight tiles (N % 256 = 128), a 1-row tile
 def test_block_fp8_ragged(M, N, K):
     run(M, N, K, seed=M)
 

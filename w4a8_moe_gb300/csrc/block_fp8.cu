@@ -12,19 +12,28 @@
 // NBUF TMEM partial buffers let the MMAs run up to NBUF K-blocks ahead of the
 // fold.
 //
-// Roles (4 + 4*NFW warps): warp 0 streams the weight tiles [128 x 128] (it
+// Roles (4 + 4*NFW warps): warp 0 streams the weight tiles [WN x 128] (it
 // starts before the dependency wait: no kernel of the call writes the
 // weights), warp 2 the activation tiles [BN x 128] and, into a ring of their
 // own that only the epilogue releases, the BN activation scales of each
-// K-block; warps 1 and 3 own TMEM and issue the MMAs, whose commit alone frees
-// a weight/activation slot; warps 4.. fold (NFW warps per 32-lane TMEM
-// quadrant, each BN/NFW of the token columns: with more warps in flight the
-// latency of each K-block's TMEM load, scale load and barrier round trip is
-// hidden by the other warps' work). Swapped operands: M = 128 weight rows,
-// N = BN tokens. With 128-token tiles one thread issues every MMA (an N = 128
-// MMA outlasts its issue) and warp 3 instead turns each landed scale slot, in
-// place, into the combined scales xs[m, g] * Wsi[nb, g], so the fold warps
-// need not each form them.
+// K-block; warps 1 and 3 own TMEM and issue the MMAs of alternate K-blocks,
+// whose commit alone frees a weight/activation slot; warps 4.. fold (NFW
+// warps per 32-lane TMEM quadrant, each a share of the partial product's
+// columns).
+//
+// Two orientations. Up to 64 tokens (decode-sized calls) the MMA is
+// M = 128 weight rows x N = BN tokens: a lane holds a weight row and its
+// columns are tokens, so each column has its own activation scale (read from
+// the scale slot as pairs and multiplied by the block's Wsi). For 128-token
+// tiles the tokens are the MMA's M (the TMEM lanes) and N = WN weight rows
+// (256 where N allows, else 128): every column a warp folds lies in one
+// weight block, so a lane needs one combined scale per K-block,
+// xs[m, g] * Wsi[n/128, g], and the fold is a TMEM load and one packed FMA
+// per pair of columns. Each lane then writes its token's row segment with
+// 32-byte stores (one whole L2 sector each). Against the weight-row
+// orientation at 128 tokens this took the [16384, 2560] projection of 4096
+// tokens from 330 to about 200 us: that fold was bound by its per-column
+// scale loads.
 //
 // When K is split over several CTAs, each writes its fp32 partial and bumps a
 // per-tile counter; the CTA that completes the count sums the partials in
@@ -47,33 +56,39 @@ struct BlkParams {
     uint32_t* err;
 };
 
-template <int BN, int PST, int NFW>
+template <int BN, int PST, int NFW, int WN>
 struct BlkTraits {
-    static constexpr int kA = 128 * 128;                  // weight tile
+    // 128-token tiles put the tokens on the TMEM lanes (MMA M = 128 tokens,
+    // N = WN weight rows); smaller token tiles are the MMA's N (M = 128
+    // weight rows)
+    static constexpr bool TL = (BN == 128);
+    static constexpr int kA = WN * 128;                   // weight tile (WN rows)
     static constexpr int kB = BN * 128;                   // activation tile
     static constexpr int kStage = kA + kB;
-    static constexpr int kNbuf = (512 / BN) < 8 ? (512 / BN) : 8;   // TMEM partial buffers
+    static constexpr int kCols = TL ? WN : BN;            // TMEM columns of one partial product
+    static constexpr int kNbuf = (512 / kCols) < 8 ? (512 / kCols) : 8;   // TMEM partial buffers
     static constexpr int kNs = PST + kNbuf;               // scale ring depth
     static constexpr int kSBytes = BN * 4;                               // one scale slot's copy
     static constexpr int kSStride = ((kSBytes + 127) / 128) * 128;       // TMA destinations: 128-byte aligned
     static constexpr int kData = PST * kStage + ((kNs * kSStride + 1023) / 1024) * 1024;
-    static constexpr int kBars = 3 * PST + 3 * kNs + 2 * kNbuf + 2;
-    // warp 3: a second MMA issuer, or (128-token tiles) the combined-scale warp
-    static constexpr bool kScaleWarp = (BN >= 128);
-    static constexpr int kIssuers = kScaleWarp ? 1 : 2;
-    // the two MMA-issuing threads take alternate K-blocks: every ring slot and
-    // partial buffer must always belong to the same thread (parity waits)
+    static constexpr int kBars = 3 * PST + 2 * kNs + 2 * kNbuf + 2;
+    // the two MMA-issuing threads (warps 1 and 3) take alternate K-blocks:
+    // every ring slot and partial buffer must always belong to the same
+    // thread (parity waits)
     static_assert(PST % 2 == 0 && kNbuf % 2 == 0, "even ring depths for two issuers");
     static constexpr int kSmem = 1024 + kData + kBars * 8 + 32;
-    static constexpr int kTmemNeed = kNbuf * BN;
+    static constexpr int kTmemNeed = kNbuf * kCols;
     static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
                                    : kTmemNeed <= 256 ? 256 : 512;
     static constexpr int kFold = 4 * NFW;                 // fold warps
     static constexpr int kThreads = 32 * (4 + kFold);
-    static constexpr int kHalf = BN / NFW;                // token columns per fold warp
-    static constexpr int kChunk = kHalf < 32 ? kHalf : 32;
+    static constexpr int kHalf = kCols / NFW;             // columns per fold warp
+    static constexpr int kChunk = kHalf < 32 ? kHalf : (TL && WN == 256 ? 16 : 32);
     static_assert(NFW == 2 || NFW == 4, "fold warps per TMEM lane quadrant");
+    static_assert(WN == 128 || (TL && WN == 256), "weight tiles of 128 rows, or 256 with tokens on the lanes");
+    static_assert(kHalf <= 128 && 128 % kHalf == 0, "a fold warp's columns lie in one weight block");
     static_assert(kHalf >= 8 && kHalf % 8 == 0, "fold columns per warp");
+    static_assert(!TL || kHalf % 16 == 0, "tokens on the lanes: 32-byte output stores");
     static_assert(kB % 1024 == 0, "stage alignment");
     static_assert((PST * kStage) % 1024 == 0 && kSStride % 128 == 0, "TMA destination alignment");
     static_assert(kSmem <= 232448, "shared memory budget");
@@ -103,6 +118,14 @@ __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c)
     uint64_t d;
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
     return d;
+}
+
+// 32-byte store (address 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void* dst, const uint32_t (&v)[8])
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(v[0]), "r"(v[1]),
+                 "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
 }
 
 // Barrier over `nthreads` threads (named barrier `id`) that returns whether
@@ -150,12 +173,13 @@ __device__ __forceinline__ void tmem_ld_cols<8>(uint32_t taddr, uint32_t* r)
                  : "r"(taddr));
 }
 
-template <int BN, int PST, int NFW>
+template <int BN, int PST, int NFW, int WN>
 __global__ void __launch_bounds__(32 * (4 + 4 * NFW), 1)
     blk_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                     const __grid_constant__ CUtensorMap tm_s, const BlkParams p)
 {
-    using Tr = BlkTraits<BN, PST, NFW>;
+    using Tr = BlkTraits<BN, PST, NFW, WN>;
+    constexpr bool TL = Tr::TL;
     constexpr int NBUF = Tr::kNbuf;
     // token tiles of 128 are used only without a K split (the host picks
     // ksplit = 1 for them), so their reduction needs no register array
@@ -171,8 +195,7 @@ __global__ void __launch_bounds__(32 * (4 + 4 * NFW), 1)
     uint64_t* sempty = xfull + PST;     // weight + activation slot free (MMA commit)
     uint64_t* sfull = sempty + PST;     // scales landed  [NS]
     uint64_t* sfree = sfull + NS;       // scales consumed by the fold  [NS]
-    uint64_t* sready = sfree + NS;      // combined scales written (scale warp)  [NS]
-    uint64_t* dfull = sready + NS;      // partial product ready  [NBUF]
+    uint64_t* dfull = sfree + NS;       // partial product ready  [NBUF]
     uint64_t* dempty = dfull + NBUF;    // partial buffer folded  [NBUF]
     uint64_t* drain = dempty + NBUF;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain + 2);   // one drain barrier per issuer
@@ -191,7 +214,6 @@ __global__ void __launch_bounds__(32 * (4 + 4 * NFW), 1)
         for (int i = 0; i < NS; ++i) {
             mbar_init(smem_u32(&sfull[i]), 1);
             mbar_init(smem_u32(&sfree[i]), Tr::kFold);
-            mbar_init(smem_u32(&sready[i]), 1);
         }
         for (int i = 0; i < NBUF; ++i) {
             mbar_init(smem_u32(&dfull[i]), 1);
@@ -255,7 +277,7 @@ __global__ void __launch_bounds__(32 * (4 + 4 * NFW), 1)
                     if (wprod) {
                         const uint32_t fb = smem_u32(&wfull[ps]);
                         mbar_arrive_expect_tx(fb, Tr::kA);
-                        tma_load_2d_hint(smem_u32(st), &tm_w, g * 128, nb * 128, fb, pol_w);
+                        tma_load_2d_hint(smem_u32(st), &tm_w, g * 128, nb * WN, fb, pol_w);
                     } else {
                         const uint32_t fb = smem_u32(&xfull[ps]);
                         mbar_arrive_expect_tx(fb, Tr::kB);
@@ -296,7 +318,7 @@ __global__ void __launch_bounds__(32 * (4 + 4 * NFW), 1)
                         mbar_wait(smem_u32(&sfull[s]), (s_last_par >> s) & 1u);
             }
         }
-    } else if (warp == 1 || (!Tr::kScaleWarp && warp == 3)) {
+    } else if (warp == 1 || warp == 3) {
         // ------------------------------------------------------------ MMA issuers
         // Every K-block has its own partial buffer, so two threads can issue:
         // warp 1 takes the even K-blocks of the CTA's sequence, warp 3 the odd
@@ -304,13 +326,13 @@ __global__ void __launch_bounds__(32 * (4 + 4 * NFW), 1)
         // (short N = 16..64 MMAs); for 128-token tiles warp 1 issues them all.
         if (lane == 0) {
             const int me = (warp == 1) ? 0 : 1;
-            const uint32_t idesc = idesc_e4m3_f32(128, BN);
+            const uint32_t idesc = idesc_e4m3_f32(128, Tr::kCols);
             int ps = 0;
             uint32_t ph = 0, kc = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 for (int kb = 0; kb < p.kb_per_split; ++kb, ++kc) {
-                    if (static_cast<int>(kc % Tr::kIssuers) != me) {
+                    if (static_cast<int>(kc % 2) != me) {
                         if (++ps == PST) {
                             ps = 0;
                             ph ^= 1u;
@@ -326,9 +348,12 @@ __global__ void __launch_bounds__(32 * (4 + 4 * NFW), 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a0 = smem_u32(smem + ps * Tr::kStage);
-                    const uint32_t b0 = a0 + Tr::kA;
-                    const uint32_t dt = tmem + static_cast<uint32_t>(d * BN);
+                    // TL: the token tile is the MMA's A (128 TMEM lanes), the
+                    // weight tile its B; otherwise the other way round
+                    const uint32_t wt = smem_u32(smem + ps * Tr::kStage);
+                    const uint32_t a0 = TL ? wt + Tr::kA : wt;
+                    const uint32_t b0 = TL ? wt : wt + Tr::kA;
+                    const uint32_t dt = tmem + static_cast<uint32_t>(d * Tr::kCols);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         umma_f8(dt, desc_kmajor_sw128(a0 + kk * 32), desc_kmajor_sw128(b0 + kk * 32),
@@ -347,44 +372,6 @@ __global__ void __launch_bounds__(32 * (4 + 4 * NFW), 1)
                 mbar_wait(smem_u32(&drain[me]), 0);
             }
         }
-    } else if (Tr::kScaleWarp && warp == 3) {
-        // ------------------------------------------------------------ combined scales
-        // sc[m] = xs[m, g] * Wsi[nb, g] (fp32, round to nearest: the product the
-        // fold would form), written over the landed activation scales; the
-        // slot is refilled by TMA only after every fold warp released it.
-        int ss = 0;
-        uint32_t sph = 0;
-        bool ok = true;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            const int nb = t / per_nb, ks = (t % per_nb) % p.ksplit;
-            for (int kb = 0; kb < p.kb_per_split; ++kb) {
-                if (!mbar_wait_or_abort<2000u>(smem_u32(&sfull[ss]), sph, s_abort)) {
-                    ok = false;
-                    break;
-                }
-                const int g = ks * p.kb_per_split + kb;
-                const float ws = __ldg(p.wsi + static_cast<int64_t>(nb) * p.KB + g);
-                float4* xs4 = reinterpret_cast<float4*>(sring + ss * Tr::kSStride);
-                if (4 * lane < BN) {
-                    float4 v = xs4[lane];
-                    v.x *= ws;
-                    v.y *= ws;
-                    v.z *= ws;
-                    v.w *= ws;
-                    xs4[lane] = v;
-                }
-                fence_proxy_async_smem();   // ordered before the slot's next TMA fill
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(smem_u32(&sready[ss]));
-                if (++ss == NS) {
-                    ss = 0;
-                    sph ^= 1u;
-                }
-            }
-        }
-        if (!ok)
-            fail();
     } else if (warp >= 4) {
         // ------------------------------------------------------------ fold + store
         grid_dep_wait();   // the partials and counters are this call's workspace
@@ -408,17 +395,25 @@ __global__ void __launch_bounds__(32 * (4 + 4 * NFW), 1)
                 const int d = static_cast<int>(kc % NBUF);
                 const uint32_t use = kc / NBUF;
                 if (!mbar_wait_or_abort(smem_u32(&dfull[d]), use & 1u, s_abort) ||
-                    !mbar_wait_or_abort(smem_u32(Tr::kScaleWarp ? &sready[ss] : &sfull[ss]), sph, s_abort)) {
+                    !mbar_wait_or_abort(smem_u32(&sfull[ss]), sph, s_abort)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const int g = ks * p.kb_per_split + kb;
-                const float ws = __ldg(p.wsi + static_cast<int64_t>(nb) * p.KB + g);
+                // the weight block of this warp's columns
+                const int wb = TL ? (nb * WN + c0) >> 7 : nb;
+                const float ws = __ldg(p.wsi + static_cast<int64_t>(wb) * p.KB + g);
                 const uint64_t ws2 = f2_pack(ws, ws);
                 const float* xs = reinterpret_cast<const float*>(sring + ss * Tr::kSStride);
                 const uint32_t tb = tmem + (static_cast<uint32_t>(q * 32) << 16) +
-                                    static_cast<uint32_t>(d * BN + c0);
+                                    static_cast<uint32_t>(d * Tr::kCols + c0);
+                // TL: this lane's token has one scale for the warp's row of
+                // partial products (all its columns are rows of weight block wb)
+                float sc_row = 0.0f;
+                if constexpr (TL)
+                    sc_row = xs[q * 32 + lane] * ws;
+                const uint64_t sc_row2 = f2_pack(sc_row, sc_row);
 #pragma unroll
                 for (int ch = 0; ch < Tr::kHalf / Tr::kChunk; ++ch) {
                     uint32_t v[Tr::kChunk];
@@ -427,7 +422,7 @@ __global__ void __launch_bounds__(32 * (4 + 4 * NFW), 1)
                     const uint64_t* xs2 = reinterpret_cast<const uint64_t*>(xs + c0 + ch * Tr::kChunk);
 #pragma unroll
                     for (int c = 0; c < Tr::kChunk / 2; ++c) {
-                        const uint64_t sc = Tr::kScaleWarp ? xs2[c] : f2_mul(xs2[c], ws2);
+                        const uint64_t sc = TL ? sc_row2 : f2_mul(xs2[c], ws2);
                         const uint64_t pv = f2_pack(__uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1]));
                         acc2[ch * Tr::kChunk / 2 + c] = f2_fma(pv, sc, acc2[ch * Tr::kChunk / 2 + c]);
                     }
@@ -447,6 +442,27 @@ __global__ void __launch_bounds__(32 * (4 + 4 * NFW), 1)
 #pragma unroll
             for (int c = 0; c < Tr::kHalf / 2; ++c)
                 f2_unpack(acc2[c], acc[2 * c], acc[2 * c + 1]);
+            if constexpr (TL) {
+                // one token row per lane, kHalf consecutive outputs of it:
+                // 32-byte stores (one whole L2 sector) of 16 bf16 each (never
+                // split over K)
+                if (!ok)
+                    break;
+                const int m = mt * BN + q * 32 + lane;
+                if (m < p.M) {
+                    uint16_t* dst = p.y + static_cast<int64_t>(m) * p.N + nb * WN + c0;
+#pragma unroll
+                    for (int c = 0; c < Tr::kHalf / 16; ++c) {
+                        uint32_t o[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            o[j] = float_to_bf16_bits(acc[16 * c + 2 * j]) |
+                                   (static_cast<uint32_t>(float_to_bf16_bits(acc[16 * c + 2 * j + 1])) << 16);
+                        st_global_v8(dst + 16 * c, o);
+                    }
+                }
+                continue;
+            }
             const int n = nb * 128 + q * 32 + lane;
             if (p.ksplit == 1) {
                 if (!ok)
@@ -586,12 +602,12 @@ BlkConfig blk_pick_config(int M, int N, int K, int num_sms)
     return c;
 }
 
-template <int BN, int PST, int NFW>
+template <int BN, int PST, int NFW, int WN>
 static int launch_blk(const CUtensorMap& tw, const CUtensorMap& tx, const CUtensorMap& ts,
                       const BlkParams& prm, int grid, cudaStream_t s)
 {
-    using Tr = BlkTraits<BN, PST, NFW>;
-    auto kern = blk_gemm_kernel<BN, PST, NFW>;
+    using Tr = BlkTraits<BN, PST, NFW, WN>;
+    auto kern = blk_gemm_kernel<BN, PST, NFW, WN>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Tr::kSmem) != cudaSuccess)
         return kErrLaunch;
     return launch_dependent(kern, dim3(grid), dim3(Tr::kThreads), Tr::kSmem, s, tw, tx, ts, prm) == cudaSuccess
@@ -603,8 +619,11 @@ int launch_block_gemm(const BlkLaunch& L, const BlkConfig& cfg, int num_sms, cud
 {
     const int BN = cfg.bn;
     const int KB = L.K / 128;
+    // 128-token tiles take 256 weight rows where N allows: the same bytes per
+    // stage feed twice the MMA work of a 128-row tile
+    const int WN = (BN == 128 && L.N % 256 == 0) ? 256 : 128;
     CUtensorMap tw, tx, ts;
-    if (!encode_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.w, L.K, L.N, L.K, 128, 128,
+    if (!encode_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.w, L.K, L.N, L.K, 128, WN,
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.xq, L.K, L.M, L.K, 128, BN,
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -619,7 +638,7 @@ int launch_block_gemm(const BlkLaunch& L, const BlkConfig& cfg, int num_sms, cud
     p.ksplit = cfg.ksplit;
     p.kb_per_split = KB / cfg.ksplit;
     p.mt_count = (L.M + BN - 1) / BN;
-    p.nb_count = L.N / 128;
+    p.nb_count = L.N / WN;
     p.wsi = L.wsi;
     p.ypart = L.ypart;
     p.tile_cnt = L.tile_cnt;
@@ -630,10 +649,12 @@ int launch_block_gemm(const BlkLaunch& L, const BlkConfig& cfg, int num_sms, cud
     const int64_t tiles = static_cast<int64_t>(p.nb_count) * p.mt_count * p.ksplit;
     const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
     switch (BN) {
-    case 16: return launch_blk<16, 8, 2>(tw, tx, ts, p, grid, s);
-    case 32: return launch_blk<32, 8, 2>(tw, tx, ts, p, grid, s);
-    case 64: return launch_blk<64, 8, 2>(tw, tx, ts, p, grid, s);
-    default: return launch_blk<128, 6, 4>(tw, tx, ts, p, grid, s);
+    case 16: return launch_blk<16, 8, 2, 128>(tw, tx, ts, p, grid, s);
+    case 32: return launch_blk<32, 8, 2, 128>(tw, tx, ts, p, grid, s);
+    case 64: return launch_blk<64, 8, 2, 128>(tw, tx, ts, p, grid, s);
+    default:
+        return WN == 256 ? launch_blk<128, 4, 2, 256>(tw, tx, ts, p, grid, s)
+                         : launch_blk<128, 6, 2, 128>(tw, tx, ts, p, grid, s);
     }
 }
 
