@@ -119,9 +119,9 @@ def throughput(world: int, tokens_per_rank: int, steps: int, ms_slowest: float) 
 NCU_TRAFFIC = {
     "sources": ["w4a8_moe_gb300/csrc/moe.cu", "w4a8_moe_gb300/csrc/ptx.cuh", "w4a8_moe_gb300/csrc/sched.cuh",
                 "w4a8_moe_gb300/csrc/internal.h"],
-    "sha256": "e19025028ed6dd85715727453857e3c28f06c61d8ae4f15ecc60863a9535ff63",
-    "grok_prefill:gate_up": 18544088064 + 2107783680,
-    "mixtral_decode:one_launch": 705905408 + 4946432,
+    "sha256": "0fa0f8003798c621afca26f5e7e2a00fb2d482ba2a4c49740c4bb6c56c45eb40",
+    "grok_prefill:gate_up": 10536430336 + 2116380416,
+    "mixtral_decode:one_launch": 705905152 + 5031936,
 }
 
 

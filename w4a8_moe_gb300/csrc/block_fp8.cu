@@ -30,10 +30,10 @@
 // weight block, so a lane needs one combined scale per K-block,
 // xs[m, g] * Wsi[n/128, g], and the fold is a TMEM load and one packed FMA
 // per pair of columns. Each lane then writes its token's row segment with
-// 32-byte stores (one whole L2 sector each). Against the weight-row
-// orientation at 128 tokens this took the [16384, 2560] projection of 4096
-// tokens from 330 to about 200 us: that fold was bound by its per-column
-// scale loads.
+// 32-byte stores (one whole L2 sector each, marked evict-first). Against the
+// weight-row orientation at 128 tokens this took the [16384, 2560]
+// projection of 4096 tokens from 330 to about 190 us: that fold was bound by
+// its per-column scale loads.
 //
 // When K is split over several CTAs, each writes its fp32 partial and bumps a
 // per-tile counter; the CTA that completes the count sums the partials in
@@ -120,11 +120,13 @@ __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c)
     return d;
 }
 
-// 32-byte store (address 32-byte aligned).
-__device__ __forceinline__ void st_global_v8(void* dst, const uint32_t (&v)[8])
+// 32-byte store (address 32-byte aligned) with an L2 cache policy and no L1
+// allocation.
+__device__ __forceinline__ void st_global_v8(void* dst, const uint32_t (&v)[8], uint64_t pol)
 {
-    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(v[0]), "r"(v[1]),
-                 "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+    asm volatile("st.global.L1::no_allocate.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;" ::"l"(
+                     dst),
+                 "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "l"(pol)
                  : "memory");
 }
 
@@ -445,11 +447,13 @@ __global__ void __launch_bounds__(32 * (4 + 4 * NFW), 1)
             if constexpr (TL) {
                 // one token row per lane, kHalf consecutive outputs of it:
                 // 32-byte stores (one whole L2 sector) of 16 bf16 each (never
-                // split over K)
+                // split over K), marked first to leave L2, where the weights
+                // and activations of the tiles in flight are reused
                 if (!ok)
                     break;
                 const int m = mt * BN + q * 32 + lane;
                 if (m < p.M) {
+                    const uint64_t pol_y = policy_evict_first();
                     uint16_t* dst = p.y + static_cast<int64_t>(m) * p.N + nb * WN + c0;
 #pragma unroll
                     for (int c = 0; c < Tr::kHalf / 16; ++c) {
@@ -458,7 +462,7 @@ __global__ void __launch_bounds__(32 * (4 + 4 * NFW), 1)
                         for (int j = 0; j < 8; ++j)
                             o[j] = float_to_bf16_bits(acc[16 * c + 2 * j]) |
                                    (static_cast<uint32_t>(float_to_bf16_bits(acc[16 * c + 2 * j + 1])) << 16);
-                        st_global_v8(dst + 16 * c, o);
+                        st_global_v8(dst + 16 * c, o, pol_y);
                     }
                 }
                 continue;

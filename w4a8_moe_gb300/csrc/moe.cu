@@ -698,6 +698,12 @@ __global__ void __launch_bounds__(32 * (4 + NCONV + NEPI), 1)
             fail();
     } else if (warp >= Tr::kEpi0) {
         // ------------------------------------------------------------ epilogue
+        // Prefill: the intermediate and the fp32 partial sums are read back by
+        // later kernels, long after L2 could hold them, so their stores are
+        // marked first to leave L2 (it keeps the operand panels the tiles in
+        // flight share). The one-launch decode reads both back from L2 soon
+        // after: plain stores there.
+        const uint64_t pol_out = policy_evict_first();
         const int q = warp & 3;
         const int sub = (warp - Tr::kEpi0) >> 2;   // chunk phase: 32-column chunks sub, sub + NEPI/4, ...
         constexpr int kChStep = NEPI / 4;
@@ -784,7 +790,11 @@ __global__ void __launch_bounds__(32 * (4 + NCONV + NEPI), 1)
                             } else {
                                 // hq = E4M3(h / a2): IEEE division, then one RNE rounding
                                 const uint32_t code = cvt_e4m3(__fdiv_rn(h, a2));
-                                p.hq[static_cast<int64_t>(pos) * p.I + kperm(i)] = static_cast<uint8_t>(code);
+                                uint8_t* dst = p.hq + static_cast<int64_t>(pos) * p.I + kperm(i);
+                                if constexpr (Tr::kA8)
+                                    st_u8_hint(dst, code, pol_out);
+                                else
+                                    *dst = static_cast<uint8_t>(code);
                                 if constexpr (!Tr::kA8)
                                     s512[cc] = e4m3_times512_f32(code);
                             }
@@ -848,8 +858,12 @@ __global__ void __launch_bounds__(32 * (4 + NCONV + NEPI), 1)
 #pragma unroll
                     for (int cc = 0; cc < 32; ++cc) {
                         const int col = ch * 32 + cc;
-                        if (col < ti.ntok && slot >= 0)
-                            yb[static_cast<int64_t>(col) * p.H] = __uint_as_float(v[cc]);
+                        if (col < ti.ntok && slot >= 0) {
+                            if constexpr (Tr::kA8)
+                                st_f32_hint(yb + static_cast<int64_t>(col) * p.H, __uint_as_float(v[cc]), pol_out);
+                            else
+                                yb[static_cast<int64_t>(col) * p.H] = __uint_as_float(v[cc]);
+                        }
                     }
                 }
             }

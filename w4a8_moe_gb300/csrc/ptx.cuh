@@ -194,6 +194,15 @@ __device__ __forceinline__ uint64_t policy_evict_last()
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
+// Global stores carrying an L2 cache policy (from createpolicy).
+__device__ __forceinline__ void st_u8_hint(uint8_t* dst, uint32_t v, uint64_t pol)
+{
+    asm volatile("st.global.L2::cache_hint.u8 [%0], %1, %2;" ::"l"(dst), "r"(v), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void st_f32_hint(float* dst, float v, uint64_t pol)
+{
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(dst), "f"(v), "l"(pol) : "memory");
+}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
