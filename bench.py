@@ -119,9 +119,9 @@ def throughput(world: int, tokens_per_rank: int, steps: int, ms_slowest: float) 
 NCU_TRAFFIC = {
     "sources": ["w4a8_moe_gb300/csrc/moe.cu", "w4a8_moe_gb300/csrc/ptx.cuh", "w4a8_moe_gb300/csrc/sched.cuh",
                 "w4a8_moe_gb300/csrc/internal.h"],
-    "sha256": "0fa0f8003798c621afca26f5e7e2a00fb2d482ba2a4c49740c4bb6c56c45eb40",
-    "grok_prefill:gate_up": 10536430336 + 2116380416,
-    "mixtral_decode:one_launch": 705905152 + 5031936,
+    "sha256": "475706d13472960100289bf9e1830467b661da4391f879be690aed80089a5713",
+    "grok_prefill:gate_up": 11102663936 + 2117626112,
+    "mixtral_decode:one_launch": 705904896 + 4948736,
 }
 
 

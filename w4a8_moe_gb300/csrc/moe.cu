@@ -897,10 +897,11 @@ __global__ void __launch_bounds__(128) moe_gather_kernel(const uint8_t* __restri
                                                          long long* __restrict__ s0x,
                                                          unsigned long long* __restrict__ s0h,
                                                          unsigned int* __restrict__ hmax, int* __restrict__ done,
-                                                         int E)
+                                                         int E, int sums)
 {
     // one block per assignment row: every 16-byte chunk of the row is in
-    // flight at once
+    // flight at once. sums = 0 (weights unpacked ahead as signed codes): the
+    // GEMMs need no exact row sums, and only the copy is done.
     __shared__ long long red[4];
     grid_dep_wait();
     grid_dep_launch();
@@ -913,6 +914,25 @@ __global__ void __launch_bounds__(128) moe_gather_kernel(const uint8_t* __restri
     const int t = __ldg(sorted_ids + pos) / k;
     const uint4* src = reinterpret_cast<const uint4*>(xq + static_cast<int64_t>(t) * H);
     uint4* dst = reinterpret_cast<uint4*>(xp + static_cast<int64_t>(pos) * H);
+    if (!sums) {
+        // rows of at most 4 chunks per thread: all loads issued first
+        constexpr int U = 4;
+        for (int c0 = threadIdx.x; c0 < H / 16; c0 += U * blockDim.x) {
+            uint4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (c0 + u * static_cast<int>(blockDim.x) < H / 16)
+                    v[u] = __ldg(src + c0 + u * blockDim.x);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int c = c0 + u * static_cast<int>(blockDim.x);
+                if (c < H / 16)
+                    dst[c] = make_uint4(prmt(v[u].x, v[u].y, 0x6420u), prmt(v[u].x, v[u].y, 0x7531u),
+                                        prmt(v[u].z, v[u].w, 0x6420u), prmt(v[u].z, v[u].w, 0x7531u));
+            }
+        }
+        return;
+    }
     int s = 0;
     for (int c = threadIdx.x; c < H / 16; c += blockDim.x) {
         const uint4 v = __ldg(src + c);
@@ -1343,10 +1363,11 @@ int launch_moe_forward(const MoeLaunch& L, const MoeConfig& cfg, int num_sms, cu
                                L.w_gu, L.w_d, L.E, L.H, L.I, L.counts, L.wq8, L.wq8 + static_cast<int64_t>(L.E) * 2 *
                                                                                         L.I * L.H) != cudaSuccess)
         return kErrLaunch;
-    // activations: gather + exact per-token sums
+    // activations: gather (+ exact per-token sums for the in-GEMM unpack)
     const bool fused = cfg.fused && !L.dynamic;
     if (launch_dependent(moe_gather_kernel, dim3(A), dim3(128), 0, s, L.xq, L.H, L.k, L.sorted_ids, A, L.xp,
-                         L.s0x, L.s0h, L.dynamic ? L.hmax : nullptr, fused ? L.done : nullptr, L.E) != cudaSuccess)
+                         L.s0x, L.s0h, L.dynamic ? L.hmax : nullptr, fused ? L.done : nullptr, L.E,
+                         a8 ? 0 : 1) != cudaSuccess)
         return kErrLaunch;
 
     // weight boxes: 64-byte rows (64-byte swizzle) for KC = 128, else 128-byte rows
