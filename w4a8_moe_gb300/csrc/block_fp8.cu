@@ -16,8 +16,9 @@
 // starts before the dependency wait: no kernel of the call writes the
 // weights), warp 2 the activation tiles [BN x 128] and, into a ring of their
 // own that only the epilogue releases, the BN activation scales of each
-// K-block; warps 1 and 3 own TMEM and issue the MMAs of alternate K-blocks,
-// whose commit alone frees a weight/activation slot; warps 4.. fold (NFW
+// K-block; warp 1 owns TMEM and with warp 3 (one issuer when the ring
+// depth is odd) issues the MMAs of alternate K-blocks, whose commit alone
+// frees a weight/activation slot; warps 4.. fold (NFW
 // warps per 32-lane TMEM quadrant, each a share of the partial product's
 // columns).
 //
@@ -29,11 +30,14 @@
 // (256 where N allows, else 128): every column a warp folds lies in one
 // weight block, so a lane needs one combined scale per K-block,
 // xs[m, g] * Wsi[n/128, g], and the fold is a TMEM load and one packed FMA
-// per pair of columns. Each lane then writes its token's row segment with
-// 32-byte stores (one whole L2 sector each, marked evict-first). Against the
-// weight-row orientation at 128 tokens this took the [16384, 2560]
-// projection of 4096 tokens from 330 to about 190 us: that fold was bound by
-// its per-column scale loads.
+// per pair of columns. With 256 weight rows each fold warp then writes its
+// [32 x 128] block through shared memory with TMA stores (a ring of 3 stages
+// leaves room for the staging and measured as fast as 4); with 128 each lane
+// writes its token's row segment with 32-byte stores (one whole L2 sector
+// each). Both are marked evict-first in L2. Against the weight-row
+// orientation at 128 tokens this took the [16384, 2560] projection of 4096
+// tokens from 330 to about 185 us: that fold was bound by its per-column
+// scale loads.
 //
 // When K is split over several CTAs, each writes its fp32 partial and bumps a
 // per-tile counter; the CTA that completes the count sums the partials in
@@ -70,25 +74,33 @@ struct BlkTraits {
     static constexpr int kNs = PST + kNbuf;               // scale ring depth
     static constexpr int kSBytes = BN * 4;                               // one scale slot's copy
     static constexpr int kSStride = ((kSBytes + 127) / 128) * 128;       // TMA destinations: 128-byte aligned
-    static constexpr int kData = PST * kStage + ((kNs * kSStride + 1023) / 1024) * 1024;
+    static constexpr int kFold = 4 * NFW;                 // fold warps
+    static constexpr int kHalf = kCols / NFW;             // columns per fold warp
+    // 256-row weight tiles write their output through shared memory with TMA
+    // stores: per fold warp a [32 rows x kHalf] bf16 block, as boxes of 64
+    // columns (128 bytes, 128-byte swizzle)
+    static constexpr bool kTmaOut = TL && WN == 256;
+    static constexpr int kOutWarp = kTmaOut ? 32 * kHalf * 2 : 0;
+    static constexpr int kSRing = ((kNs * kSStride + 1023) / 1024) * 1024;
+    static constexpr int kData = PST * kStage + kSRing + kFold * kOutWarp;
     static constexpr int kBars = 3 * PST + 2 * kNs + 2 * kNbuf + 2;
-    // the two MMA-issuing threads (warps 1 and 3) take alternate K-blocks:
-    // every ring slot and partial buffer must always belong to the same
-    // thread (parity waits)
-    static_assert(PST % 2 == 0 && kNbuf % 2 == 0, "even ring depths for two issuers");
+    // With an even ring depth the two MMA-issuing threads (warps 1 and 3) take
+    // alternate K-blocks: every ring slot and partial buffer must always
+    // belong to the same thread (parity waits). An odd ring has one issuer.
+    static constexpr int kIssuers = (PST % 2 == 0) ? 2 : 1;
+    static_assert(kNbuf % kIssuers == 0, "partial buffers per issuer");
     static constexpr int kSmem = 1024 + kData + kBars * 8 + 32;
     static constexpr int kTmemNeed = kNbuf * kCols;
     static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
                                    : kTmemNeed <= 256 ? 256 : 512;
-    static constexpr int kFold = 4 * NFW;                 // fold warps
     static constexpr int kThreads = 32 * (4 + kFold);
-    static constexpr int kHalf = kCols / NFW;             // columns per fold warp
     static constexpr int kChunk = kHalf < 32 ? kHalf : (TL && WN == 256 ? 16 : 32);
     static_assert(NFW == 2 || NFW == 4, "fold warps per TMEM lane quadrant");
     static_assert(WN == 128 || (TL && WN == 256), "weight tiles of 128 rows, or 256 with tokens on the lanes");
     static_assert(kHalf <= 128 && 128 % kHalf == 0, "a fold warp's columns lie in one weight block");
     static_assert(kHalf >= 8 && kHalf % 8 == 0, "fold columns per warp");
     static_assert(!TL || kHalf % 16 == 0, "tokens on the lanes: 32-byte output stores");
+    static_assert(!kTmaOut || kHalf % 64 == 0, "TMA output boxes of 64 columns");
     static_assert(kB % 1024 == 0, "stage alignment");
     static_assert((PST * kStage) % 1024 == 0 && kSStride % 128 == 0, "TMA destination alignment");
     static_assert(kSmem <= 232448, "shared memory budget");
@@ -178,7 +190,8 @@ __device__ __forceinline__ void tmem_ld_cols<8>(uint32_t taddr, uint32_t* r)
 template <int BN, int PST, int NFW, int WN>
 __global__ void __launch_bounds__(32 * (4 + 4 * NFW), 1)
     blk_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
-                    const __grid_constant__ CUtensorMap tm_s, const BlkParams p)
+                    const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_y,
+                    const BlkParams p)
 {
     using Tr = BlkTraits<BN, PST, NFW, WN>;
     constexpr bool TL = Tr::TL;
@@ -191,6 +204,7 @@ __global__ void __launch_bounds__(32 * (4 + 4 * NFW), 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
     uint8_t* sring = smem + PST * Tr::kStage;
+    uint8_t* sout = sring + Tr::kSRing;    // output staging, kOutWarp bytes per fold warp
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Tr::kData);
     uint64_t* wfull = bars;             // weight tile landed
     uint64_t* xfull = wfull + PST;      // activation tile landed
@@ -230,6 +244,8 @@ __global__ void __launch_bounds__(32 * (4 + 4 * NFW), 1)
         prefetch_tmap(&tm_w);
         prefetch_tmap(&tm_x);
         prefetch_tmap(&tm_s);
+        if constexpr (Tr::kTmaOut)
+            prefetch_tmap(&tm_y);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(s_tmem), Tr::kTmemCols);
@@ -320,12 +336,12 @@ __global__ void __launch_bounds__(32 * (4 + 4 * NFW), 1)
                         mbar_wait(smem_u32(&sfull[s]), (s_last_par >> s) & 1u);
             }
         }
-    } else if (warp == 1 || warp == 3) {
+    } else if (warp == 1 || (Tr::kIssuers == 2 && warp == 3)) {
         // ------------------------------------------------------------ MMA issuers
         // Every K-block has its own partial buffer, so two threads can issue:
         // warp 1 takes the even K-blocks of the CTA's sequence, warp 3 the odd
         // ones, which hides each thread's barrier waits behind the other's MMAs
-        // (short N = 16..64 MMAs); for 128-token tiles warp 1 issues them all.
+        // (short N = 16..64 MMAs). With an odd ring depth warp 1 issues them all.
         if (lane == 0) {
             const int me = (warp == 1) ? 0 : 1;
             const uint32_t idesc = idesc_e4m3_f32(128, Tr::kCols);
@@ -334,7 +350,7 @@ __global__ void __launch_bounds__(32 * (4 + 4 * NFW), 1)
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 for (int kb = 0; kb < p.kb_per_split; ++kb, ++kc) {
-                    if (static_cast<int>(kc % 2) != me) {
+                    if (static_cast<int>(kc % Tr::kIssuers) != me) {
                         if (++ps == PST) {
                             ps = 0;
                             ph ^= 1u;
@@ -451,6 +467,40 @@ __global__ void __launch_bounds__(32 * (4 + 4 * NFW), 1)
                 // and activations of the tiles in flight are reused
                 if (!ok)
                     break;
+                if constexpr (Tr::kTmaOut) {
+                    // Through shared memory: the warp's [32 x kHalf] block as
+                    // boxes of 64 columns, 128-byte swizzled (16-byte chunk j of
+                    // row r at position j ^ (r % 8): conflict-free writes), then
+                    // TMA stores of whole rows (rows past M are not written).
+                    uint8_t* stg = sout + (warp - 4) * Tr::kOutWarp;
+                    if (lane == 0)
+                        bulk_wait_read_all();   // the previous tile's stores have read it
+                    __syncwarp();
+#pragma unroll
+                    for (int b = 0; b < Tr::kHalf / 64; ++b) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const float* a8v = acc + 64 * b + 8 * j;
+                            uint4 o;
+                            o.x = float_to_bf16_bits(a8v[0]) | (static_cast<uint32_t>(float_to_bf16_bits(a8v[1])) << 16);
+                            o.y = float_to_bf16_bits(a8v[2]) | (static_cast<uint32_t>(float_to_bf16_bits(a8v[3])) << 16);
+                            o.z = float_to_bf16_bits(a8v[4]) | (static_cast<uint32_t>(float_to_bf16_bits(a8v[5])) << 16);
+                            o.w = float_to_bf16_bits(a8v[6]) | (static_cast<uint32_t>(float_to_bf16_bits(a8v[7])) << 16);
+                            *reinterpret_cast<uint4*>(stg + b * 4096 + lane * 128 + ((j ^ (lane & 7)) << 4)) = o;
+                        }
+                    }
+                    fence_proxy_async_smem();   // the writes, before the async proxy reads them
+                    __syncwarp();
+                    if (lane == 0) {
+                        const uint64_t pol_y = policy_evict_first();
+#pragma unroll
+                        for (int b = 0; b < Tr::kHalf / 64; ++b)
+                            tma_store_2d_hint(&tm_y, nb * WN + c0 + 64 * b, mt * BN + q * 32, smem_u32(stg + b * 4096),
+                                              pol_y);
+                        bulk_commit_group();
+                    }
+                    continue;
+                }
                 const int m = mt * BN + q * 32 + lane;
                 if (m < p.M) {
                     const uint64_t pol_y = policy_evict_first();
@@ -544,6 +594,12 @@ __global__ void __launch_bounds__(32 * (4 + 4 * NFW), 1)
         }
         if (!ok)
             fail();
+        if constexpr (Tr::kTmaOut) {
+            // the staging must outlive the stores that read it
+            if (lane == 0)
+                bulk_wait_all();
+            __syncwarp();
+        }
     }
 
     tc_fence_before();
@@ -607,14 +663,14 @@ BlkConfig blk_pick_config(int M, int N, int K, int num_sms)
 }
 
 template <int BN, int PST, int NFW, int WN>
-static int launch_blk(const CUtensorMap& tw, const CUtensorMap& tx, const CUtensorMap& ts,
+static int launch_blk(const CUtensorMap& tw, const CUtensorMap& tx, const CUtensorMap& ts, const CUtensorMap& ty,
                       const BlkParams& prm, int grid, cudaStream_t s)
 {
     using Tr = BlkTraits<BN, PST, NFW, WN>;
     auto kern = blk_gemm_kernel<BN, PST, NFW, WN>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Tr::kSmem) != cudaSuccess)
         return kErrLaunch;
-    return launch_dependent(kern, dim3(grid), dim3(Tr::kThreads), Tr::kSmem, s, tw, tx, ts, prm) == cudaSuccess
+    return launch_dependent(kern, dim3(grid), dim3(Tr::kThreads), Tr::kSmem, s, tw, tx, ts, ty, prm) == cudaSuccess
                ? kOK
                : kErrLaunch;
 }
@@ -626,7 +682,7 @@ int launch_block_gemm(const BlkLaunch& L, const BlkConfig& cfg, int num_sms, cud
     // 128-token tiles take 256 weight rows where N allows: the same bytes per
     // stage feed twice the MMA work of a 128-row tile
     const int WN = (BN == 128 && L.N % 256 == 0) ? 256 : 128;
-    CUtensorMap tw, tx, ts;
+    CUtensorMap tw, tx, ts, ty;
     if (!encode_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.w, L.K, L.N, L.K, 128, WN,
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.xq, L.K, L.M, L.K, 128, BN,
@@ -634,6 +690,15 @@ int launch_block_gemm(const BlkLaunch& L, const BlkConfig& cfg, int num_sms, cud
         !encode_map_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, L.xs_t, L.ld_t, KB,
                        static_cast<uint64_t>(L.ld_t) * 4, BN, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
         return kErrLaunch;
+    // bf16 output [M, N] for the TMA stores of 256-row weight tiles: boxes of
+    // 64 columns x 32 rows, 128-byte swizzle (unused by the other shapes)
+    if (WN == 256) {
+        if (!encode_map_2d(&ty, CU_TENSOR_MAP_DATA_TYPE_UINT16, L.y, L.N, L.M, static_cast<uint64_t>(L.N) * 2, 64, 32,
+                           CU_TENSOR_MAP_SWIZZLE_128B))
+            return kErrLaunch;
+    } else {
+        ty = tx;
+    }
     BlkParams p{};
     p.M = L.M;
     p.N = L.N;
@@ -653,12 +718,14 @@ int launch_block_gemm(const BlkLaunch& L, const BlkConfig& cfg, int num_sms, cud
     const int64_t tiles = static_cast<int64_t>(p.nb_count) * p.mt_count * p.ksplit;
     const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
     switch (BN) {
-    case 16: return launch_blk<16, 8, 2, 128>(tw, tx, ts, p, grid, s);
-    case 32: return launch_blk<32, 8, 2, 128>(tw, tx, ts, p, grid, s);
-    case 64: return launch_blk<64, 8, 2, 128>(tw, tx, ts, p, grid, s);
+    case 16: return launch_blk<16, 8, 2, 128>(tw, tx, ts, ty, p, grid, s);
+    case 32: return launch_blk<32, 8, 2, 128>(tw, tx, ts, ty, p, grid, s);
+    case 64: return launch_blk<64, 8, 2, 128>(tw, tx, ts, ty, p, grid, s);
     default:
-        return WN == 256 ? launch_blk<128, 4, 2, 256>(tw, tx, ts, p, grid, s)
-                         : launch_blk<128, 6, 2, 128>(tw, tx, ts, p, grid, s);
+        // 256-row tiles: a ring of 3 stages (the 4th measured no faster) and
+        // 64 KB of output staging
+        return WN == 256 ? launch_blk<128, 3, 2, 256>(tw, tx, ts, ty, p, grid, s)
+                         : launch_blk<128, 6, 2, 128>(tw, tx, ts, ty, p, grid, s);
     }
 }
 
