@@ -119,9 +119,9 @@ def throughput(world: int, tokens_per_rank: int, steps: int, ms_slowest: float) 
 NCU_TRAFFIC = {
     "sources": ["w4a8_moe_gb300/csrc/moe.cu", "w4a8_moe_gb300/csrc/ptx.cuh", "w4a8_moe_gb300/csrc/sched.cuh",
                 "w4a8_moe_gb300/csrc/internal.h"],
-    "sha256": "475706d13472960100289bf9e1830467b661da4391f879be690aed80089a5713",
-    "grok_prefill:gate_up": 11102663936 + 2117626112,
-    "mixtral_decode:one_launch": 705904896 + 4948736,
+    "sha256": "b86d8b9602552df2fbaa7c0a4eabafbca38720537e2cb7d8d0c1e56f3f330512",
+    "grok_prefill:gate_up": 12511229440 + 2116034304,
+    "mixtral_decode:one_launch": 705904384 + 5035520,
 }
 
 
