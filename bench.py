@@ -114,12 +114,13 @@ def throughput(world: int, tokens_per_rank: int, steps: int, ms_slowest: float) 
 # (summarized with their commands under profiles/), valid only for the GEMM
 # sources they were taken on: moe.cu without its row kernels (gather,
 # intermediate quantizer, combine: the part from "// Gather:" up to
-# "// Host side"), and the headers the GEMM includes, comments left out. A
-# changed GEMM reports null.
+# "// Host side"), the PTX and scheduling headers the GEMM includes, and the
+# moe.cu section of internal.h, comments left out. A changed GEMM reports
+# null.
 NCU_TRAFFIC = {
     "sources": ["w4a8_moe_gb300/csrc/moe.cu", "w4a8_moe_gb300/csrc/ptx.cuh", "w4a8_moe_gb300/csrc/sched.cuh",
                 "w4a8_moe_gb300/csrc/internal.h"],
-    "sha256": "b86d8b9602552df2fbaa7c0a4eabafbca38720537e2cb7d8d0c1e56f3f330512",
+    "sha256": "4407a13aeb1d6637c0459af119d757763f477085095cd7fea663cfce2ea8e27f",
     "grok_prefill:gate_up": 12511229440 + 2116034304,
     "mixtral_decode:one_launch": 705904384 + 5035520,
 }
@@ -137,6 +138,9 @@ def gemm_source_digest(read=None) -> str:
         if f.endswith("moe.cu"):
             a, b = data.index(b"// Gather: "), data.index(b"// Host side")
             data = data[:a] + data[b:]
+        if f.endswith("internal.h"):
+            a = data.index(b"// ---- moe.cu")
+            data = data[a:data.index(b"// ---- ", a + 1)]
         text = re.sub(r"/\*.*?\*/", "", data.decode(), flags=re.S)
         text = re.sub(r"//[^\n]*", "", text)
         code = "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
