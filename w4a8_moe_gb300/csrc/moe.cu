@@ -1160,10 +1160,32 @@ __global__ void __launch_bounds__(256) moe_finalize_kernel(
     if (!live)
         return;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    if constexpr (KS_MAX == 1) {
+        // one partial per assignment: every assignment's partial requested
+        // before the first is added
+        float4 v[KPRE];
 #pragma unroll
-    for (int j = 0; j < KPRE; ++j)
-        if (j < k)
-            fin_accumulate<KS_MAX>(acc, pos_p[j], wt_p[j], sd_p[j], a2, A, H, n, ksplit, ypart, s0h, pmul);
+        for (int j = 0; j < KPRE; ++j)
+            if (j < k)
+                v[j] = __ldg(reinterpret_cast<const float4*>(ypart + static_cast<int64_t>(pos_p[j]) * H + n));
+#pragma unroll
+        for (int j = 0; j < KPRE; ++j) {
+            if (j < k) {
+                const float shift =
+                    s0h ? static_cast<float>(static_cast<long long>(__ldg(s0h + pos_p[j]))) * (1.0f / 64.0f) : 0.0f;
+                const float Pv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+                const float Sv[4] = {sd_p[j].x, sd_p[j].y, sd_p[j].z, sd_p[j].w};
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    acc[c] = fmaf(wt_p[j], a2 * Sv[c] * fmaf(pmul, Pv[c], -shift), acc[c]);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < KPRE; ++j)
+            if (j < k)
+                fin_accumulate<KS_MAX>(acc, pos_p[j], wt_p[j], sd_p[j], a2, A, H, n, ksplit, ypart, s0h, pmul);
+    }
     for (int j = KPRE; j < k; ++j) {
         const int a = t * k + j;
         const int e = __ldg(ids + a);
