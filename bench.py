@@ -120,9 +120,9 @@ def throughput(world: int, tokens_per_rank: int, steps: int, ms_slowest: float) 
 NCU_TRAFFIC = {
     "sources": ["w4a8_moe_gb300/csrc/moe.cu", "w4a8_moe_gb300/csrc/ptx.cuh", "w4a8_moe_gb300/csrc/sched.cuh",
                 "w4a8_moe_gb300/csrc/internal.h"],
-    "sha256": "4407a13aeb1d6637c0459af119d757763f477085095cd7fea663cfce2ea8e27f",
-    "grok_prefill:gate_up": 12511229440 + 2116034304,
-    "mixtral_decode:one_launch": 705904384 + 5035520,
+    "sha256": "53d58d5cfe022ee6aa66c4e0bab6853ec02489eb9603ebc8109b957d6fa66c93",
+    "grok_prefill:gate_up": 11414465792 + 2116776192,
+    "mixtral_decode:one_launch": 705904640 + 4985856,
 }
 
 

@@ -145,6 +145,7 @@ struct MoeWs {
     unsigned int* hmax;    // header word at byte 64 (dynamic only)
     int* done;             // [256] per-expert progress counters (one-launch forward)
     uint8_t* wq8;          // prefill: the weights unpacked once per call
+    int* sync;             // prefill: the down GEMM's pacing counters
 };
 static size_t moe_ws(int T, int H, int I, int E, int k, MoeWs* w, void* ws, bool dynamic = false)
 {
@@ -158,6 +159,7 @@ static size_t moe_ws(int T, int H, int I, int E, int k, MoeWs* w, void* ws, bool
     w->hf = c.take<float>(dynamic ? A * I * 4 : 0);
     w->done = c.take<int>(256 * 4);
     w->wq8 = c.take<uint8_t>(moe_unpack_once(T) ? static_cast<size_t>(E) * 3 * I * H : 0);
+    w->sync = c.take<int>(moe_unpack_once(T) ? static_cast<size_t>(kMoeSyncInts) * 4 : 0);
     w->hmax = ws ? reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + 64) : nullptr;
     return c.off;
 }
@@ -462,6 +464,7 @@ static int moe_forward_common(const uint8_t* x_e4m3, const float* a1_scale, int 
     L.ypart = w.ypart;
     L.done = w.done;
     L.wq8 = w.wq8;
+    L.sync = w.sync;
     // header words 48 and 49: the one-launch forward's claim counters, zero
     // when the workspace is allocated and left zero by every call
     L.claim = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + 192);

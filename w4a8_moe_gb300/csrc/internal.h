@@ -57,6 +57,14 @@ cudaError_t launch_route_gate(const uint16_t* x, const uint16_t* gate, int T, in
 
 // ---- moe.cu
 constexpr int kMaxKsplit = 16;   // largest split of the down projection's K
+// Prefill down GEMM pacing: a CTA's weight stream passes checkpoint c (every
+// kMoeSyncEvery stages) only after every CTA passed checkpoint c - kMoeSyncSlack
+// (or finished), so the CTAs sharing L2-resident panels stay within a few
+// dozen K-stages of each other. kMoeSyncInts counters: checkpoints, then the
+// count of CTAs done.
+constexpr int kMoeSyncInts = 1024;
+constexpr int kMoeSyncEvery = 32;
+constexpr int kMoeSyncSlack = 2;
 
 struct MoeConfig {
     int bn;        // token tile (MMA N upper bound)
@@ -86,6 +94,7 @@ struct MoeLaunch {
     uint8_t* xp; long long* s0x; uint8_t* hq; unsigned long long* s0h; float* ypart;
     uint8_t* wq8;  // unpacked weights [E, 2I, H] (gate_up, tile row order) then [E, H, I]
     int* done;  // [E] per-expert gate_up progress of the one-launch forward
+    int* sync;  // prefill: [kMoeSyncInts] the down GEMM's pacing counters (zeroed by the gather)
     int* claim; // [2] its tile-claim counters (zero between calls)
     // dynamic intermediate scale (moe_w4a8_forward_dynamic): h in fp32, its
     // max as float bits, the scale written to a2_out

@@ -85,6 +85,8 @@ struct MoeGemmParams {
     // rows for `band` token tiles at a time, down all token tiles for `band`
     // weight-row tiles at a time (band2: the down tiles of MODE 3)
     int band, band2;
+    // prefill down GEMM: pacing counters (see kMoeSyncEvery), nullptr: none
+    int* sync;
     uint32_t* err;
 };
 
@@ -435,6 +437,9 @@ __global__ void __launch_bounds__(32 * (4 + NCONV + NEPI), 1)
             uint32_t last_par = 0;     // bit s: parity of the last fill of slot s
             bool ok = true;
             int seen = -1;   // MODE 3: experts up to this one have all their gate_up tiles written
+            // prefill down GEMM pacing (weight producer): stages issued so far
+            const bool pace = (MODE == 1) && wprod && p.sync != nullptr;
+            uint32_t gst = 0;
             TileSeq wi;
             for (start_seq(wi, wprod ? 0 : 1); wi.valid() && ok;) {
                 const int t = wi.t;
@@ -460,6 +465,19 @@ __global__ void __launch_bounds__(32 * (4 + NCONV + NEPI), 1)
                 for (int kb = wi.kb0; kb < wi.kb0 + wi.nkb; ++kb) {
                     if (wi.claim_here(kb, 4))
                         wi.claim_next();
+                    if (pace && gst % kMoeSyncEvery == 0) {
+                        const int c = static_cast<int>(gst / kMoeSyncEvery);
+                        if (c < kMoeSyncInts - 1) {
+                            if (c >= kMoeSyncSlack &&
+                                !pace_wait_or_abort(p.sync + (c - kMoeSyncSlack), p.sync + (kMoeSyncInts - 1),
+                                                    static_cast<int>(gridDim.x), s_abort)) {
+                                ok = false;
+                                break;
+                            }
+                            atomicAdd(p.sync + c, 1);
+                        }
+                    }
+                    ++gst;
                     if (!mbar_wait_or_abort<kHint>(smem_u32(&freeb[s]), ph ^ 1u, s_abort)) {
                         ok = false;
                         break;
@@ -508,6 +526,8 @@ __global__ void __launch_bounds__(32 * (4 + NCONV + NEPI), 1)
                 if (ok)   // (after a failed wait nothing more is published)
                     wi.next();
             }
+            if (pace)
+                atomicAdd(p.sync + (kMoeSyncInts - 1), 1);   // this CTA's weight stream is done
             if constexpr (MODE == 3) {
                 if (wprod) {
                     // this CTA makes no further claim; the last CTA to get here
@@ -897,7 +917,7 @@ __global__ void __launch_bounds__(128) moe_gather_kernel(const uint8_t* __restri
                                                          long long* __restrict__ s0x,
                                                          unsigned long long* __restrict__ s0h,
                                                          unsigned int* __restrict__ hmax, int* __restrict__ done,
-                                                         int E, int sums)
+                                                         int E, int sums, int* __restrict__ sync)
 {
     // one block per assignment row: every 16-byte chunk of the row is in
     // flight at once. sums = 0 (weights unpacked ahead as signed codes): the
@@ -910,6 +930,9 @@ __global__ void __launch_bounds__(128) moe_gather_kernel(const uint8_t* __restri
     if (done && blockIdx.x == 0)
         for (int e = threadIdx.x; e < E; e += blockDim.x)
             done[e] = 0;   // per-expert gate_up progress of the one-launch forward
+    if (sync && blockIdx.x == 1 % gridDim.x)
+        for (int i = threadIdx.x; i < kMoeSyncInts; i += blockDim.x)
+            sync[i] = 0;   // the prefill down GEMM's pacing counters
     const int pos = blockIdx.x;
     const int t = __ldg(sorted_ids + pos) / k;
     const uint4* src = reinterpret_cast<const uint4*>(xq + static_cast<int64_t>(t) * H);
@@ -1389,7 +1412,7 @@ int launch_moe_forward(const MoeLaunch& L, const MoeConfig& cfg, int num_sms, cu
     const bool fused = cfg.fused && !L.dynamic;
     if (launch_dependent(moe_gather_kernel, dim3(A), dim3(128), 0, s, L.xq, L.H, L.k, L.sorted_ids, A, L.xp,
                          L.s0x, L.s0h, L.dynamic ? L.hmax : nullptr, fused ? L.done : nullptr, L.E,
-                         a8 ? 0 : 1) != cudaSuccess)
+                         a8 ? 0 : 1, (a8 && !fused) ? L.sync : nullptr) != cudaSuccess)
         return kErrLaunch;
 
     // weight boxes: 64-byte rows (64-byte swizzle) for KC = 128, else 128-byte rows
@@ -1493,6 +1516,7 @@ int launch_moe_forward(const MoeLaunch& L, const MoeConfig& cfg, int num_sms, cu
     dn.streamk = cfg.streamk;
     dn.nslots = cfg.nslots;
     dn.band = a8 ? kPrefillBand : 0;
+    dn.sync = a8 ? L.sync : nullptr;
     tiles = static_cast<int64_t>(dn.rt_count) * tok_tiles_max * dn.ksplit;
     grid = cfg.streamk ? num_sms : static_cast<int>(tiles < num_sms ? tiles : num_sms);
     st = dispatch_gemm<1>(cfg, tw_d, tb_d, tw_d, tb_d, dn, grid, s);

@@ -160,6 +160,23 @@ __device__ __forceinline__ bool counter_wait_or_abort(const int* counter, int ta
     return ok;
 }
 
+// Bounded wait until *passed + *done >= target (both counters only grow).
+__device__ __forceinline__ bool pace_wait_or_abort(const int* passed, const int* done, int target,
+                                                   const volatile int* abort)
+{
+    bool ok = ld_acquire_gpu(passed) + ld_acquire_gpu(done) >= target;
+    if (!ok) {
+        const long long t0 = clock64();
+        for (uint32_t it = 0; it < kWaitMaxPolls && !ok; ++it) {
+            if (*abort || clock64() - t0 > kWaitBudgetCycles)
+                break;
+            __nanosleep(64);
+            ok = ld_acquire_gpu(passed) + ld_acquire_gpu(done) >= target;
+        }
+    }
+    return ok;
+}
+
 // ---------------------------------------------------------------- TMA
 // 2-D tile load global -> shared, completion counted on an mbarrier in bytes.
 // c0 is the innermost coordinate (elements), c1 the row.
