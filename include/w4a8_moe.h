@@ -166,13 +166,15 @@ size_t moe_route_gate_workspace_size(int T, int H, int E, int k);
  *   Requires H and I positive multiples of 128, 1 <= k <= E <= 256, T >= 1.
  *   ws: moe_w4a8_workspace_size(T, H, I, E, k) bytes. Above 128 tokens this
  *       includes E * 3 * I * H bytes where the call unpacks the INT4 weights of
- *       the experts with tokens once (to E4M3 operand bytes) before the GEMMs.
+ *       the experts with tokens once (to E4M3 operand bytes) before the GEMMs,
+ *       and 4 KB of pacing counters for the down GEMM.
  * Up to 128 tokens both projections run in one persistent launch (one CTA per
  * SM; see moe_w4a8_plan) whose down tiles wait for the gate_up tiles of the
- * same expert in other CTAs. Those waits assume every CTA of the launch gets an
- * SM within the bounded-wait budget (about 2 s): kernels on other streams that
- * hold SMs for longer make the call report W4A8_ERR_TIMEOUT through
- * w4a8_device_error instead of hanging.
+ * same expert in other CTAs; above 128 tokens the CTAs of the down launch pace
+ * their weight streams against each other (grid-wide checkpoints). Those waits
+ * assume every CTA of the launch gets an SM within the bounded-wait budget
+ * (about 2 s): kernels on other streams that hold SMs for longer make the call
+ * report W4A8_ERR_TIMEOUT through w4a8_device_error instead of hanging.
  */
 int moe_w4a8_forward(const uint8_t* x_e4m3, const float* a1_scale, int T, int H, int I, int E,
                      int k, const int32_t* w_gu, const float* s_gu, const int32_t* w_d,
