@@ -43,7 +43,9 @@
 //   sum_h x_h q_h = 512 * sum_h x_h dec(o_h) - 8 * sum_h x_h,
 // where the per-token sum_h x_h is exact integer bookkeeping (S0 below). The
 // tensor-core product is the exact upcast the pages describe, shifted by a
-// constant that the epilogue removes.
+// constant that the epilogue removes. That is the in-GEMM form (decode-sized
+// calls). Prefill-sized calls unpack the weights once per call instead, to the
+// E4M3 code of q itself (every INT4 value is exact in E4M3), and need no shift.
 #include "internal.h"
 #include "ptx.cuh"
 #include "sched.cuh"
