@@ -82,6 +82,23 @@ def test_empty_experts_and_one_hot_expert():
     run_case(case1, what="one expert")
 
 
+def test_prefill_empty_experts_and_one_hot_expert():
+    """The prefill plan (weights unpacked ahead, banded tiles, paced down
+    weight streams) with idle experts, and with every token on one expert."""
+    T, E = 600, 8
+    logits = torch.randn(T, E, generator=torch.Generator().manual_seed(5))
+    logits[:, 1] = -50.0           # never routed
+    logits[:, 5] = -50.0
+    case = MoECase(T, 384, 640, E, 2, 1, logits_override=logits)
+    assert case.o_counts[1] == 0 and case.o_counts[5] == 0
+    run_case(case, what="prefill empty experts")
+    logits1 = torch.zeros(T, E)
+    logits1[:, 4] = 20.0           # every token on expert 4 (k = 1)
+    case1 = MoECase(T, 384, 640, E, 1, 0, logits_override=logits1)
+    assert case1.o_counts[4] == T
+    run_case(case1, what="prefill one expert")
+
+
 def test_deterministic_and_error_word_clean():
     import w4a8_moe_gb300 as lib
     case = MoECase(37, 512, 512, 8, 2, 1, seed=9)
