@@ -115,6 +115,21 @@ def test_deterministic_and_error_word_clean():
     assert int(ws[192:200].count_nonzero()) == 0
 
 
+def test_prefill_deterministic_across_calls():
+    """Prefill plan: repeated calls on one workspace give identical bits (the
+    down launch's pacing counters are reset by every call) and leave the
+    error word clean."""
+    import w4a8_moe_gb300 as lib
+    T, H, I, E, k = 700, 384, 640, 8, 2
+    case = MoECase(T, H, I, E, k, 1, seed=12)
+    assert lib.moe_w4a8_plan(T, H, I, E, k)["one_launch"] == 0
+    ws = torch.zeros(lib.moe_w4a8_workspace_size(T, H, I, E, k), dtype=torch.uint8, device="cuda")
+    outs = [case.run_gpu(ws=ws).clone() for _ in range(3)]
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+    assert lib.w4a8_device_error(ws) == 0
+
+
 def covering_sample(case: MoECase, n: int, seed: int = 0):
     """A seeded sample of n tokens that covers every expert with tokens: first
     one token of each expert, least loaded expert first, then random tokens,
